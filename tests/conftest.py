@@ -1,0 +1,42 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the libdcp kernels)")
+    config.addinivalue_line("markers", "slow: long-running case")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built():
+    import oracle
+    import synth
+    oracle.build()
+    synth.build()
+    if os.path.exists(os.path.join(ROOT, "__graft_entry__.py")):
+        import __graft_entry__
+        __graft_entry__.build()
+    yield
+
+
+def has_gpu() -> bool:
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+@pytest.fixture
+def gpu():
+    if not has_gpu():
+        pytest.skip("no CUDA device")
+    import torch
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")
