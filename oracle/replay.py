@@ -1,4 +1,4 @@
-"""Host replay of a workload's eviction schedule with the oracle, and host<->device copies of caches.
+"""Host replay of a workload's eviction schedule with the oracle, and ulp comparisons of stored values.
 
 TEST INFRASTRUCTURE ONLY (tests/, __graft_entry__.smoke(), bench.py's CPU baseline).  Seeded contents come from the
 ``synth`` generator; every state transition here is the oracle's.
@@ -66,45 +66,6 @@ def state_before_last(w: Workload, head_is_static=None):
         if cc not in placed:
             place_chunk(hc, w, cc)
     return hc, ev[-1]
-
-
-# ------------------------------------------------------------------------------------------ device copies
-def dcp_config(w: Workload):
-    import autoregressive_video_diffusion_gb300 as dcp
-    return dcp.Config(gamma=w.gamma, keep_rule=0, sink_chunks=w.sink_chunks, window_chunks=w.window_chunks,
-                      tokens_per_frame=w.tokens_per_frame, frames_per_chunk=w.frames_per_chunk,
-                      n_temporal_pairs=w.n_temporal_pairs, rope_base=w.rope_base, g_recent_R=w.R, g_span_S=w.S,
-                      g_mode=w.g_mode, max_frames=w.max_frames)
-
-
-def _to_torch(a: np.ndarray, w: Workload):
-    import torch
-    if w.dtype == 0:
-        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
-    return torch.from_numpy(a)
-
-
-def to_device(hc: HostCache, w: Workload):
-    import torch
-
-    import autoregressive_video_diffusion_gb300 as dcp
-    dev = dcp.KVCache(w.L, w.H, w.D, w.dtype, w.cap, w.hist_cap)
-    dev.k.copy_(_to_torch(hc.k, w))
-    dev.v.copy_(_to_torch(hc.v, w))
-    dev.hist_len.copy_(torch.from_numpy(hc.hist_len))
-    dev.hist_t.copy_(torch.from_numpy(hc.hist_t))
-    return dev
-
-
-def from_device(dev, w: Workload) -> HostCache:
-    import torch
-    if w.dtype == 0:
-        k = dev.k.view(torch.int16).cpu().numpy().view(np.uint16)
-        v = dev.v.view(torch.int16).cpu().numpy().view(np.uint16)
-    else:
-        k = dev.k.cpu().numpy()
-        v = dev.v.cpu().numpy()
-    return HostCache(k, v, dev.hist_len.cpu().numpy(), dev.hist_t.cpu().numpy(), w.hist_cap)
 
 
 # ------------------------------------------------------------------------------------------ comparisons
