@@ -1,0 +1,256 @@
+"""Python binding of libdcp, the GB300 (sm_103a) DeCoPrune history-KV prune step.
+
+Argument marshalling only: every function here passes tensor addresses and sizes to the C ABI declared in
+``include/dcp.h`` (same names) on torch's current CUDA stream, and raises :class:`DcpError` on a non-zero status.
+Every step of the prune runs in the library's CUDA kernels; there is no CPU or PyTorch fallback, and importing this
+package fails if ``libdcp.so`` has not been built (``python autoregressive_video_diffusion_gb300/build.py``).
+
+The method (page "DeCoPrune이 디노이징 불일치로 비디오 KV 캐시를 85% 줄인다", onedev.kr/papers/726): score each
+token of the chunk that leaves the dense window by l = (1/d)||x0hat(tau*) - x_final||^2, keep the tokens with
+l > gamma (one mask for every layer), physically gather K[m], V[m] into the compacted history, and re-index the
+temporal RoPE phase of history keys to t~(t) = q0 - g(q0 - t).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdcp.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python autoregressive_video_diffusion_gb300/build.py` "
+                      "(nvcc, sm_103a).  There is no fallback implementation.")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+DCP_OK, DCP_EINVAL, DCP_ECAPACITY, DCP_ECUDA, DCP_ETIMEOUT, DCP_EDEVICE = range(6)
+DCP_BF16, DCP_F32 = 0, 1
+
+# The page's fixed choices (section "premises and limits"): 4-step schedule, probe at zero-based index 2, gamma.
+SCHEDULE = (999, 957, 899, 702)
+PROBE_INDEX = 2
+TAU_STAR = SCHEDULE[PROBE_INDEX]
+GAMMA = 0.10
+
+
+class DcpCacheC(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("L", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("dtype", ctypes.c_int32), ("cap", ctypes.c_int64),
+                ("hist_cap", ctypes.c_int64), ("hist_len", ctypes.c_void_p), ("hist_t", ctypes.c_void_p),
+                ("status", ctypes.c_void_p)]
+
+
+class DcpConfigC(ctypes.Structure):
+    _fields_ = [("gamma", ctypes.c_float), ("keep_rule", ctypes.c_int32), ("sink_chunks", ctypes.c_int32),
+                ("window_chunks", ctypes.c_int32), ("tokens_per_frame", ctypes.c_int32),
+                ("frames_per_chunk", ctypes.c_int32), ("n_temporal_pairs", ctypes.c_int32),
+                ("pair_layout", ctypes.c_int32), ("rope_base", ctypes.c_double), ("g_recent_R", ctypes.c_double),
+                ("g_span_S", ctypes.c_double), ("g_mode", ctypes.c_int32), ("rephase_sink", ctypes.c_int32),
+                ("max_frames", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class DcpPrCounter(ctypes.Structure):
+    _fields_ = [("visible", ctypes.c_int64), ("full", ctypes.c_int64)]
+
+
+_vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_pc, _pg = ctypes.POINTER(DcpCacheC), ctypes.POINTER(DcpConfigC)
+_SIGS = {
+    "dcp_workspace_size": ([_pc, _pg], _sz),
+    "dcp_score_workspace_size": ([_i32], _sz),
+    "dcp_workspace_init": ([_vp, _sz, _vp], _i32),
+    "dcp_score_mask": ([_vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "dcp_compact_layers": ([_pc, _pg, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp], _i32),
+    "dcp_rope_reindex": ([_pc, _pg, _i32, _i32, _vp, _sz, _vp], _i32),
+    "dcp_prune_step": ([_pc, _pg, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "dcp_workspace_outputs": ([_pc, _pg, _vp, _vp, _vp, _vp], _i32),
+    "dcp_get_status": ([_vp, _vp], _i32),
+    "dcp_reset_status": ([_vp, _vp], _i32),
+    "dcp_status_string": ([_i32], ctypes.c_char_p),
+    "dcp_pr_add_chunk": ([ctypes.POINTER(DcpPrCounter), _i64, _i64, _i64, _i64, _i64], None),
+    "dcp_pr_value": ([ctypes.POINTER(DcpPrCounter)], ctypes.c_double),
+    "dcp_abi_struct_sizes": ([], ctypes.c_uint32),
+    "dcp_set_phase_events": ([_vp, _vp], _i32),
+    "dcp_debug_force_scan_timeout": ([_i32], _i32),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+_sizes = lib.dcp_abi_struct_sizes()
+if (_sizes >> 16) != ctypes.sizeof(DcpCacheC) or (_sizes & 0xFFFF) != ctypes.sizeof(DcpConfigC):
+    raise ImportError("libdcp struct layout does not match the binding")
+
+
+class DcpError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what}: {dcp_status_string(status)} ({status})")
+        self.status = status
+
+
+def dcp_status_string(status: int) -> str:
+    return lib.dcp_status_string(status).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != DCP_OK:
+        raise DcpError(what, rc)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+@dataclass
+class Config:
+    """Method parameters (dcp_config)."""
+    gamma: float = GAMMA
+    keep_rule: int = 0
+    sink_chunks: int = 1
+    window_chunks: int = 3
+    tokens_per_frame: int = 1560
+    frames_per_chunk: int = 4
+    n_temporal_pairs: int = 22
+    rope_base: float = 10000.0
+    g_recent_R: float = 12.0
+    g_span_S: float = 24.0
+    g_mode: int = 0
+    max_frames: int = 256
+    pair_layout: int = 0
+    rephase_sink: int = 0
+
+    @property
+    def C(self) -> int:
+        return self.tokens_per_frame * self.frames_per_chunk
+
+    def c(self) -> DcpConfigC:
+        return DcpConfigC(self.gamma, self.keep_rule, self.sink_chunks, self.window_chunks, self.tokens_per_frame,
+                          self.frames_per_chunk, self.n_temporal_pairs, self.pair_layout, self.rope_base,
+                          self.g_recent_R, self.g_span_S, self.g_mode, self.rephase_sink, self.max_frames, 0)
+
+
+class KVCache:
+    """Device tensors of one KV cache in the sink | history | window-ring layout (dcp_cache)."""
+
+    def __init__(self, L: int, H: int, D: int, dtype: int, cap: int, hist_cap: int, device="cuda"):
+        tdt = torch.bfloat16 if dtype == DCP_BF16 else torch.float32
+        self.L, self.H, self.D, self.dtype, self.cap, self.hist_cap = L, H, D, dtype, cap, hist_cap
+        self.k = torch.empty((L, H, cap, D), dtype=tdt, device=device)
+        self.v = torch.empty((L, H, cap, D), dtype=tdt, device=device)
+        self.hist_len = torch.zeros(L * H, dtype=torch.int32, device=device)
+        self.hist_t = torch.zeros(max(hist_cap, 1), dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def c(self) -> DcpCacheC:
+        return DcpCacheC(_ptr(self.k), _ptr(self.v), self.L, self.H, self.D, self.dtype, self.cap, self.hist_cap,
+                         _ptr(self.hist_len), _ptr(self.hist_t), _ptr(self.status))
+
+
+def dcp_workspace_size(cache: KVCache, cfg: Config) -> int:
+    cc, gc = cache.c(), cfg.c()
+    n = lib.dcp_workspace_size(ctypes.byref(cc), ctypes.byref(gc))
+    if n == 0:
+        raise DcpError("dcp_workspace_size", DCP_EINVAL)
+    return n
+
+
+def dcp_score_workspace_size(n_tok: int) -> int:
+    return lib.dcp_score_workspace_size(n_tok)
+
+
+def dcp_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    _check(lib.dcp_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "dcp_workspace_init")
+
+
+def new_workspace(nbytes: int, device="cuda", stream=None) -> torch.Tensor:
+    """A zero-initialised, 256-byte aligned device workspace (torch allocation; not on the hot path)."""
+    ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + nbytes]
+    dcp_workspace_init(ws, stream)
+    return ws
+
+
+def dcp_score_mask(x0hat: torch.Tensor, xref: torch.Tensor, gamma: float, keep_rule: int, ell, mask, idx, kept,
+                   status: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    n_tok, d = x0hat.shape
+    _check(lib.dcp_score_mask(_ptr(x0hat), _ptr(xref), n_tok, d, gamma, keep_rule, _ptr(ell), _ptr(mask), _ptr(idx),
+                              _ptr(kept), _ptr(status), _ptr(ws), ws.numel(), _stream(stream)), "dcp_score_mask")
+
+
+def dcp_compact_layers(cache: KVCache, cfg: Config, evict_slot: int, evict_first_frame: int, mask: torch.Tensor,
+                       head_is_static, q0: int, kept, ws: torch.Tensor, stream=None) -> None:
+    cc, gc = cache.c(), cfg.c()
+    _check(lib.dcp_compact_layers(ctypes.byref(cc), ctypes.byref(gc), evict_slot, evict_first_frame, _ptr(mask),
+                                  _ptr(head_is_static), q0, _ptr(kept), _ptr(ws), ws.numel(), _stream(stream)),
+           "dcp_compact_layers")
+
+
+def dcp_rope_reindex(cache: KVCache, cfg: Config, q0_prev: int, q0: int, ws: torch.Tensor, stream=None) -> None:
+    cc, gc = cache.c(), cfg.c()
+    _check(lib.dcp_rope_reindex(ctypes.byref(cc), ctypes.byref(gc), q0_prev, q0, _ptr(ws), ws.numel(),
+                                _stream(stream)), "dcp_rope_reindex")
+
+
+def dcp_prune_step(cache: KVCache, cfg: Config, x0hat: torch.Tensor, xref: torch.Tensor, evict_slot: int,
+                   evict_first_frame: int, q0_prev: int, q0: int, head_is_static, kept_dev, kept_host_pinned,
+                   ws: torch.Tensor, stream=None) -> None:
+    cc, gc = cache.c(), cfg.c()
+    _check(lib.dcp_prune_step(ctypes.byref(cc), ctypes.byref(gc), _ptr(x0hat), _ptr(xref), x0hat.shape[1],
+                              evict_slot, evict_first_frame, q0_prev, q0, _ptr(head_is_static), _ptr(kept_dev),
+                              _ptr(kept_host_pinned), _ptr(ws), ws.numel(), _stream(stream)), "dcp_prune_step")
+
+
+def dcp_workspace_outputs(cache: KVCache, cfg: Config, ws: torch.Tensor):
+    """Views of the workspace where the last prune/compact call left l (fp32), the mask (uint8), the index list."""
+    cc, gc = cache.c(), cfg.c()
+    pe, pm, pi = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+    _check(lib.dcp_workspace_outputs(ctypes.byref(cc), ctypes.byref(gc), _ptr(ws), ctypes.byref(pe),
+                                     ctypes.byref(pm), ctypes.byref(pi)), "dcp_workspace_outputs")
+    C, base = cfg.C, ws.data_ptr()
+    ell = ws[pe.value - base: pe.value - base + 4 * C].view(torch.float32)
+    mask = ws[pm.value - base: pm.value - base + C]
+    idx = ws[pi.value - base: pi.value - base + 4 * C].view(torch.int32)
+    return ell, mask, idx
+
+
+def dcp_get_status(status: torch.Tensor, stream=None) -> int:
+    return lib.dcp_get_status(_ptr(status), _stream(stream))
+
+
+def dcp_reset_status(status: torch.Tensor, stream=None) -> None:
+    _check(lib.dcp_reset_status(_ptr(status), _stream(stream)), "dcp_reset_status")
+
+
+def dcp_pr_add_chunk(acc: DcpPrCounter, n_planes: int, hist_len_sum: int, sink_visible: int, window_visible: int,
+                     prior_tokens: int) -> None:
+    lib.dcp_pr_add_chunk(ctypes.byref(acc), n_planes, hist_len_sum, sink_visible, window_visible, prior_tokens)
+
+
+def dcp_pr_value(acc: DcpPrCounter) -> float:
+    return lib.dcp_pr_value(ctypes.byref(acc))
+
+
+def dcp_set_phase_events(ev_after_scan, ev_after_gather) -> None:
+    """Record torch.cuda.Event objects (or None) after the scan and gather kernels of each dcp_prune_step."""
+    a = None if ev_after_scan is None else ev_after_scan.cuda_event
+    b = None if ev_after_gather is None else ev_after_gather.cuda_event
+    _check(lib.dcp_set_phase_events(a, b), "dcp_set_phase_events")
+
+
+def dcp_debug_force_scan_timeout(on: bool) -> bool:
+    return bool(lib.dcp_debug_force_scan_timeout(1 if on else 0))

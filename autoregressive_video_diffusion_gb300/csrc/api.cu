@@ -1,0 +1,407 @@
+// Host side of libdcp: argument validation, workspace layout and the launch sequence of each entry point.
+// The entry points and their contracts are documented in include/dcp.h.
+#include <cmath>
+#include <cstring>
+
+#include "dcp_internal.cuh"
+
+using namespace dcp;
+
+namespace {
+
+int g_force_timeout = 0;
+cudaEvent_t g_ev_after_scan = nullptr;
+cudaEvent_t g_ev_after_gather = nullptr;
+
+struct Derived {
+  int64_t C, sink_rows, win_row0, n_planes;
+  int esize;
+  int T_s;
+  Layout lay;
+};
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+dcp_status check_cache_cfg(const dcp_cache* c, const dcp_config* g, Derived* d) {
+  if (!c || !g) return DCP_EINVAL;
+  if (!c->k || !c->v || !c->hist_len || !c->hist_t || !c->status) return DCP_EINVAL;
+  if (c->L < 1 || c->H < 1 || c->D < 2 || (c->D & 1)) return DCP_EINVAL;
+  if (c->dtype != DCP_BF16 && c->dtype != DCP_F32) return DCP_EINVAL;
+  const int es = c->dtype == DCP_BF16 ? 2 : 4;
+  if (((int64_t)c->D * es) % 16) return DCP_EINVAL;
+  if (!aligned(c->k, 16) || !aligned(c->v, 16) || !aligned(c->hist_len, 4) || !aligned(c->hist_t, 4) ||
+      !aligned(c->status, 4))
+    return DCP_EINVAL;
+  if (g->tokens_per_frame < 1 || g->frames_per_chunk < 1 || g->sink_chunks < 0 || g->window_chunks < 0)
+    return DCP_EINVAL;
+  const int64_t C = (int64_t)g->tokens_per_frame * g->frames_per_chunk;
+  if (C > (int64_t(1) << 30)) return DCP_EINVAL;
+  if (g->n_temporal_pairs < 0 || g->n_temporal_pairs > c->D / 2) return DCP_EINVAL;
+  if (g->pair_layout != 0 || g->rephase_sink != 0 || g->reserved != 0) return DCP_EINVAL;
+  if (!std::isfinite(g->rope_base) || !(g->rope_base > 0.0)) return DCP_EINVAL;
+  if (!std::isfinite(g->g_recent_R) || !std::isfinite(g->g_span_S)) return DCP_EINVAL;
+  if (g->g_mode != 0 && g->g_mode != 1) return DCP_EINVAL;
+  if (g->g_recent_R < (double)g->window_chunks * g->frames_per_chunk) return DCP_EINVAL;
+  if (g->g_mode == 0 && g->g_span_S < g->g_recent_R) return DCP_EINVAL;
+  if (g->g_mode == 1 && g->g_span_S < 0.0) return DCP_EINVAL;
+  if (g->keep_rule != 0 && g->keep_rule != 1) return DCP_EINVAL;
+  if (!std::isfinite(g->gamma)) return DCP_EINVAL;
+  if (g->max_frames < 1) return DCP_EINVAL;
+  if (c->hist_cap < 0 || c->hist_cap > INT32_MAX) return DCP_EINVAL;
+  const int64_t sink_rows = (int64_t)g->sink_chunks * C;
+  const int64_t need = sink_rows + c->hist_cap + ((int64_t)g->window_chunks + 1) * C;
+  if (c->cap < need) return DCP_EINVAL;
+  const int64_t T_s = (int64_t)g->sink_chunks * g->frames_per_chunk;
+  if (T_s > INT32_MAX) return DCP_EINVAL;
+  if (d) {
+    d->C = C;
+    d->sink_rows = sink_rows;
+    d->win_row0 = sink_rows + c->hist_cap;
+    d->n_planes = (int64_t)c->L * c->H;
+    d->esize = es;
+    d->T_s = (int)T_s;
+    d->lay = make_layout(C, d->n_planes, g->frames_per_chunk, g->n_temporal_pairs, g->max_frames);
+  }
+  return DCP_OK;
+}
+
+dcp_status check_ws(const void* ws, size_t bytes, size_t need) {
+  if (!ws || !aligned(ws, 256) || bytes < need) return DCP_EINVAL;
+  return DCP_OK;
+}
+
+dcp_status check_eviction(const dcp_config* g, const Derived& d, int32_t evict_slot, int32_t evict_first_frame,
+                          int32_t q0) {
+  if (evict_slot < 0 || evict_slot > g->window_chunks) return DCP_EINVAL;
+  if (evict_first_frame < d.T_s) return DCP_EINVAL;
+  if ((int64_t)evict_first_frame + g->frames_per_chunk > q0) return DCP_EINVAL;
+  if (q0 > g->max_frames) return DCP_EINVAL;
+  return DCP_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+void choose_tiling(int32_t d, const float* x0, const float* xr, int* lpt, int* tile) {
+  const int nvec = d / 4;
+  const bool vec_ok = d % 4 == 0 && nvec >= 1 && nvec <= 32 && (nvec & (nvec - 1)) == 0 && aligned(x0, 16) &&
+                      aligned(xr, 16);
+  if (vec_ok) {
+    *lpt = nvec;
+    *tile = 1024 / nvec < kMaxTile ? 1024 / nvec : kMaxTile;
+  } else {
+    *lpt = 0;
+    *tile = 64;
+  }
+}
+
+// Scan parameters shared by the calls that work on a cache.
+ScanParams cache_scan_params(const dcp_cache* c, const dcp_config* g, const Derived& d, void* ws) {
+  ScanParams sp{};
+  sp.gamma = g->gamma;
+  sp.keep_rule = g->keep_rule;
+  sp.ctrl = at<Ctrl>(ws, 0);
+  sp.tile_state = at<unsigned long long>(ws, d.lay.tile_state);
+  sp.status = c->status;
+  sp.force_timeout = g_force_timeout;
+  sp.hist_len = c->hist_len;
+  sp.hist_t = c->hist_t;
+  sp.n_planes = (int32_t)d.n_planes;
+  sp.hist_cap = c->hist_cap;
+  sp.T = g->tokens_per_frame;
+  sp.dyn_list = at<int32_t>(ws, d.lay.dyn_list);
+  sp.rp_list = at<int32_t>(ws, d.lay.rp_list);
+  sp.rp_len = at<int32_t>(ws, d.lay.rp_len);
+  sp.trig_g = at<float4>(ws, d.lay.trig_g);
+  sp.rot_g = at<uint8_t>(ws, d.lay.rot_g);
+  sp.trig_h = at<float4>(ws, d.lay.trig_h);
+  sp.rot_h = at<uint8_t>(ws, d.lay.rot_h);
+  sp.n_t = g->n_temporal_pairs;
+  sp.base = g->rope_base;
+  sp.R = g->g_recent_R;
+  sp.S = g->g_span_S;
+  sp.g_mode = g->g_mode;
+  sp.T_s = d.T_s;
+  return sp;
+}
+
+void finish_tables(ScanParams& sp) {
+  const int entries = (sp.g_frames + (sp.h_hi - sp.h_lo)) * sp.n_t;
+  sp.n_trig_blocks = (entries + kThreads - 1) / kThreads;
+}
+
+GatherParams gather_params(const dcp_cache* c, const dcp_config* g, const Derived& d, void* ws, int32_t slot) {
+  GatherParams gp{};
+  gp.k = static_cast<char*>(c->k);
+  gp.v = static_cast<char*>(c->v);
+  gp.row_bytes = c->D * d.esize;
+  gp.plane_bytes = c->cap * (int64_t)gp.row_bytes;
+  gp.vpr = gp.row_bytes / 16;
+  gp.vpr_shift = -1;
+  for (int s = 0; s < 31; ++s)
+    if ((1 << s) == gp.vpr) gp.vpr_shift = s;
+  gp.src_row0 = d.win_row0 + (int64_t)slot * d.C;
+  gp.dst_row0 = d.sink_rows;
+  gp.ctrl = at<Ctrl>(ws, 0);
+  gp.idx = at<int32_t>(ws, d.lay.idx);
+  gp.dyn_list = at<int32_t>(ws, d.lay.dyn_list);
+  gp.trig_g = at<float4>(ws, d.lay.trig_g);
+  gp.rot_g = at<uint8_t>(ws, d.lay.rot_g);
+  gp.T = g->tokens_per_frame;
+  gp.n_t = g->n_temporal_pairs;
+  gp.dtype = c->dtype;
+  gp.rows_per_item = 16384 / gp.row_bytes > 0 ? 16384 / gp.row_bytes : 1;
+  return gp;
+}
+
+RephaseParams rephase_params(const dcp_cache* c, const dcp_config* g, const Derived& d, void* ws, int h_lo,
+                             int h_hi) {
+  RephaseParams rp{};
+  rp.k = static_cast<char*>(c->k);
+  rp.row_bytes = c->D * d.esize;
+  rp.plane_bytes = c->cap * (int64_t)rp.row_bytes;
+  rp.nvt = (2 * g->n_temporal_pairs * d.esize + 15) / 16;
+  rp.hist_row0 = d.sink_rows;
+  rp.ctrl = at<Ctrl>(ws, 0);
+  rp.rp_list = at<int32_t>(ws, d.lay.rp_list);
+  rp.rp_len = at<int32_t>(ws, d.lay.rp_len);
+  rp.hist_t = c->hist_t;
+  rp.trig_h = at<float4>(ws, d.lay.trig_h);
+  rp.rot_h = at<uint8_t>(ws, d.lay.rot_h);
+  rp.n_t = g->n_temporal_pairs;
+  rp.dtype = c->dtype;
+  rp.h_lo = h_lo;
+  rp.h_hi = h_hi;
+  rp.status = c->status;
+  return rp;
+}
+
+dcp_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? DCP_OK : DCP_ECUDA; }
+
+}  // namespace
+
+namespace dcp {
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+}  // namespace dcp
+
+extern "C" {
+
+size_t dcp_workspace_size(const dcp_cache* cache, const dcp_config* cfg) {
+  Derived d;
+  if (check_cache_cfg(cache, cfg, &d) != DCP_OK) return 0;
+  return d.lay.total;
+}
+
+size_t dcp_score_workspace_size(int32_t n_tok) {
+  if (n_tok < 1 || n_tok > (1 << 30)) return 0;
+  return make_layout(n_tok, 0, 0, 0, 0).total;
+}
+
+dcp_status dcp_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(Ctrl)) return DCP_EINVAL;
+  return cuda_ok(cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+dcp_status dcp_score_mask(const float* x0hat, const float* xref, int32_t n_tok, int32_t d, float gamma,
+                          int32_t keep_rule, float* ell_dev, uint8_t* mask_dev, int32_t* idx_dev, int32_t* kept_dev,
+                          int32_t* status_dev, void* ws, size_t ws_bytes, void* stream) {
+  if (!x0hat || !xref || !status_dev || n_tok < 1 || n_tok > (1 << 30) || d < 1 || !std::isfinite(gamma) ||
+      (keep_rule != 0 && keep_rule != 1))
+    return DCP_EINVAL;
+  if (!aligned(status_dev, 4) || (idx_dev && !aligned(idx_dev, 4)) || (ell_dev && !aligned(ell_dev, 4)) ||
+      (kept_dev && !aligned(kept_dev, 4)) || !aligned(x0hat, 4) || !aligned(xref, 4))
+    return DCP_EINVAL;
+  const Layout lay = make_layout(n_tok, 0, 0, 0, 0);
+  if (check_ws(ws, ws_bytes, lay.total) != DCP_OK) return DCP_EINVAL;
+  ScanParams sp{};
+  sp.x0hat = x0hat;
+  sp.xref = xref;
+  sp.n_tok = n_tok;
+  sp.d = d;
+  sp.gamma = gamma;
+  sp.keep_rule = keep_rule;
+  choose_tiling(d, x0hat, xref, &sp.lpt, &sp.tile);
+  sp.n_tiles = (n_tok + sp.tile - 1) / sp.tile;
+  sp.ell_out = ell_dev;
+  sp.mask_out = mask_dev;
+  sp.idx_out = idx_dev;
+  sp.ctrl = at<Ctrl>(ws, 0);
+  sp.tile_state = at<unsigned long long>(ws, lay.tile_state);
+  sp.status = status_dev;
+  sp.kept_dev = kept_dev;
+  sp.force_timeout = g_force_timeout;
+  return cuda_ok(launch_scan(sp, (cudaStream_t)stream));
+}
+
+dcp_status dcp_compact_layers(const dcp_cache* cache, const dcp_config* cfg, int32_t evict_slot,
+                              int32_t evict_first_frame, const uint8_t* mask, const uint8_t* head_is_static,
+                              int32_t q0, int32_t* kept_dev, void* ws, size_t ws_bytes, void* stream) {
+  Derived d;
+  if (check_cache_cfg(cache, cfg, &d) != DCP_OK) return DCP_EINVAL;
+  if (check_eviction(cfg, d, evict_slot, evict_first_frame, q0) != DCP_OK) return DCP_EINVAL;
+  if (!mask || check_ws(ws, ws_bytes, d.lay.total) != DCP_OK) return DCP_EINVAL;
+  if (kept_dev && !aligned(kept_dev, 4)) return DCP_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  ScanParams sp = cache_scan_params(cache, cfg, d, ws);
+  sp.mask_in = mask;
+  sp.n_tok = (int32_t)d.C;
+  sp.tile = kMaxTile;
+  sp.lpt = 0;
+  sp.n_tiles = (int32_t)((d.C + sp.tile - 1) / sp.tile);
+  sp.mask_out = at<uint8_t>(ws, d.lay.mask);
+  sp.idx_out = at<int32_t>(ws, d.lay.idx);
+  sp.kept_dev = kept_dev;
+  sp.update_cache = 1;
+  sp.head_is_static = head_is_static;
+  sp.evict_first_frame = evict_first_frame;
+  sp.g_frames = cfg->frames_per_chunk;
+  sp.q0 = q0;
+  sp.q0_prev = q0;
+  finish_tables(sp);
+  dcp_status rc = cuda_ok(launch_scan(sp, st));
+  if (rc != DCP_OK) return rc;
+  return cuda_ok(launch_gather(gather_params(cache, cfg, d, ws, evict_slot), st));
+}
+
+dcp_status dcp_rope_reindex(const dcp_cache* cache, const dcp_config* cfg, int32_t q0_prev, int32_t q0, void* ws,
+                            size_t ws_bytes, void* stream) {
+  Derived d;
+  if (check_cache_cfg(cache, cfg, &d) != DCP_OK) return DCP_EINVAL;
+  if (q0_prev > q0 || q0 > cfg->max_frames || q0_prev < d.T_s) return DCP_EINVAL;
+  if (check_ws(ws, ws_bytes, d.lay.total) != DCP_OK) return DCP_EINVAL;
+  if (q0_prev == q0 || cfg->n_temporal_pairs == 0) return DCP_OK;  // no key changes phase
+  cudaStream_t st = (cudaStream_t)stream;
+  ScanParams sp = cache_scan_params(cache, cfg, d, ws);
+  sp.want_rephase = 1;
+  sp.h_lo = d.T_s;
+  sp.h_hi = q0;
+  sp.q0 = q0;
+  sp.q0_prev = q0_prev;
+  finish_tables(sp);
+  dcp_status rc = cuda_ok(launch_scan(sp, st));
+  if (rc != DCP_OK) return rc;
+  return cuda_ok(launch_rephase(rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi), st));
+}
+
+dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const float* x0hat, const float* xref,
+                          int32_t dd, int32_t evict_slot, int32_t evict_first_frame, int32_t q0_prev, int32_t q0,
+                          const uint8_t* head_is_static, int32_t* kept_dev, int32_t* kept_host_pinned, void* ws,
+                          size_t ws_bytes, void* stream) {
+  Derived d;
+  if (check_cache_cfg(cache, cfg, &d) != DCP_OK) return DCP_EINVAL;
+  if (check_eviction(cfg, d, evict_slot, evict_first_frame, q0) != DCP_OK) return DCP_EINVAL;
+  if (q0_prev > q0 || q0_prev < d.T_s) return DCP_EINVAL;
+  if (!x0hat || !xref || dd < 1 || !aligned(x0hat, 4) || !aligned(xref, 4)) return DCP_EINVAL;
+  if (kept_dev && !aligned(kept_dev, 4)) return DCP_EINVAL;
+  if (check_ws(ws, ws_bytes, d.lay.total) != DCP_OK) return DCP_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  const bool rephase = q0_prev != q0 && cfg->n_temporal_pairs > 0;
+  ScanParams sp = cache_scan_params(cache, cfg, d, ws);
+  sp.x0hat = x0hat;
+  sp.xref = xref;
+  sp.n_tok = (int32_t)d.C;
+  sp.d = dd;
+  choose_tiling(dd, x0hat, xref, &sp.lpt, &sp.tile);
+  sp.n_tiles = (int32_t)((d.C + sp.tile - 1) / sp.tile);
+  sp.ell_out = at<float>(ws, d.lay.ell);
+  sp.mask_out = at<uint8_t>(ws, d.lay.mask);
+  sp.idx_out = at<int32_t>(ws, d.lay.idx);
+  sp.kept_dev = kept_dev;
+  sp.update_cache = 1;
+  sp.want_rephase = rephase ? 1 : 0;
+  sp.head_is_static = head_is_static;
+  sp.evict_first_frame = evict_first_frame;
+  sp.g_frames = cfg->frames_per_chunk;
+  sp.h_lo = d.T_s;
+  sp.h_hi = rephase ? evict_first_frame : d.T_s;
+  sp.q0 = q0;
+  sp.q0_prev = q0_prev;
+  finish_tables(sp);
+  dcp_status rc = cuda_ok(launch_scan(sp, st));
+  if (rc != DCP_OK) return rc;
+  if (g_ev_after_scan && cudaEventRecord(g_ev_after_scan, st) != cudaSuccess) return DCP_ECUDA;
+  rc = cuda_ok(launch_gather(gather_params(cache, cfg, d, ws, evict_slot), st));
+  if (rc != DCP_OK) return rc;
+  if (g_ev_after_gather && cudaEventRecord(g_ev_after_gather, st) != cudaSuccess) return DCP_ECUDA;
+  if (rephase) {
+    rc = cuda_ok(launch_rephase(rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi), st));
+    if (rc != DCP_OK) return rc;
+  }
+  if (kept_host_pinned)
+    rc = cuda_ok(cudaMemcpyAsync(kept_host_pinned, &at<Ctrl>(ws, 0)->k, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  return rc;
+}
+
+dcp_status dcp_workspace_outputs(const dcp_cache* cache, const dcp_config* cfg, void* ws, float** ell_dev,
+                                 uint8_t** mask_dev, int32_t** idx_dev) {
+  Derived d;
+  if (check_cache_cfg(cache, cfg, &d) != DCP_OK || !ws) return DCP_EINVAL;
+  if (ell_dev) *ell_dev = at<float>(ws, d.lay.ell);
+  if (mask_dev) *mask_dev = at<uint8_t>(ws, d.lay.mask);
+  if (idx_dev) *idx_dev = at<int32_t>(ws, d.lay.idx);
+  return DCP_OK;
+}
+
+dcp_status dcp_get_status(const int32_t* status_dev, void* stream) {
+  if (!status_dev) return DCP_EINVAL;
+  int32_t v = 0;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DCP_ECUDA;
+  if (cudaMemcpy(&v, status_dev, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DCP_ECUDA;
+  return v;
+}
+
+dcp_status dcp_reset_status(int32_t* status_dev, void* stream) {
+  if (!status_dev) return DCP_EINVAL;
+  return cuda_ok(cudaMemsetAsync(status_dev, 0, sizeof(int32_t), (cudaStream_t)stream));
+}
+
+const char* dcp_status_string(dcp_status s) {
+  switch (s) {
+    case DCP_OK: return "ok";
+    case DCP_EINVAL: return "invalid argument";
+    case DCP_ECAPACITY: return "history capacity exceeded";
+    case DCP_ECUDA: return "CUDA runtime error";
+    case DCP_ETIMEOUT: return "index scan wait timed out";
+    case DCP_EDEVICE: return "inconsistent cache state on the device";
+    default: return "unknown status";
+  }
+}
+
+void dcp_pr_add_chunk(dcp_pr_counter* acc, int64_t n_planes, int64_t hist_len_sum, int64_t sink_tokens_visible,
+                      int64_t window_tokens_visible, int64_t prior_tokens) {
+  if (!acc) return;
+  acc->visible += n_planes * (sink_tokens_visible + window_tokens_visible) + hist_len_sum;
+  acc->full += n_planes * prior_tokens;
+}
+
+double dcp_pr_value(const dcp_pr_counter* acc) {
+  if (!acc || acc->full <= 0) return 0.0;
+  return 1.0 - (double)acc->visible / (double)acc->full;
+}
+
+dcp_status dcp_set_phase_events(void* ev_after_scan, void* ev_after_gather) {
+  g_ev_after_scan = (cudaEvent_t)ev_after_scan;
+  g_ev_after_gather = (cudaEvent_t)ev_after_gather;
+  return DCP_OK;
+}
+
+uint32_t dcp_abi_struct_sizes(void) { return ((uint32_t)sizeof(dcp_cache) << 16) | (uint32_t)sizeof(dcp_config); }
+
+int32_t dcp_debug_force_scan_timeout(int32_t on) {
+  int32_t prev = g_force_timeout;
+  g_force_timeout = on ? 1 : 0;
+  return prev;
+}
+
+}  // extern "C"

@@ -1,0 +1,230 @@
+// Internal declarations of libdcp: workspace layout, kernel parameter blocks, device helpers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dcp.h"
+
+namespace dcp {
+
+constexpr int kThreads = 256;          // every kernel of the library runs 256-thread CTAs
+constexpr int kMaxTile = 256;          // tokens per scan tile (one token per thread in the scan phase)
+constexpr int kMinTile = 32;
+constexpr uint32_t kFlagAgg = 1u;      // tile published its own count
+constexpr uint32_t kFlagPrefix = 2u;   // tile published its inclusive prefix
+constexpr int kSpinLimit = 1 << 22;    // bounded look-back wait (x ~64 ns backoff -> well under a second)
+constexpr int kForcedSpinLimit = 4096;
+
+// Control block at the start of the workspace.  Fields written by the scan kernel's final CTA are read by the
+// gather and re-index kernels that follow it on the stream.
+struct Ctrl {
+  uint32_t ticket;      // dynamic CTA numbering of the scan kernel (reset to 0 at the end of every call)
+  uint32_t done;        // CTAs of the scan kernel that finished (reset to 0 at the end of every call)
+  int32_t tile_error;   // a tile's bounded wait gave up during this call (reset by the final CTA)
+  int32_t abort;        // final verdict of the scan kernel: nonzero -> later kernels of the call do nothing
+  int32_t k;            // kept tokens
+  int32_t n_dyn;        // planes that receive the kept rows
+  int32_t common_len;   // their history length before the step
+  int32_t n_rp;         // planes with history rows to re-index
+  int32_t rp_max;       // longest such history
+  int32_t pad[55];
+};
+static_assert(sizeof(Ctrl) == 256, "ctrl block is one 256-byte line");
+
+struct Layout {           // byte offsets inside the workspace
+  size_t tile_state, ell, mask, idx, dyn_list, rp_list, rp_len, trig_g, rot_g, trig_h, rot_h, total;
+  int32_t max_tiles;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline Layout make_layout(int64_t n_tok, int64_t n_planes, int64_t F, int64_t n_t, int64_t max_frames) {
+  Layout L{};
+  size_t off = sizeof(Ctrl);
+  L.max_tiles = (int32_t)((n_tok + kMinTile - 1) / kMinTile);
+  L.tile_state = off; off = align256(off + sizeof(unsigned long long) * (size_t)L.max_tiles);
+  L.ell = off;        off = align256(off + 4 * (size_t)n_tok);
+  L.mask = off;       off = align256(off + (size_t)n_tok);
+  L.idx = off;        off = align256(off + 4 * (size_t)n_tok);
+  L.dyn_list = off;   off = align256(off + 4 * (size_t)n_planes);
+  L.rp_list = off;    off = align256(off + 4 * (size_t)n_planes);
+  L.rp_len = off;     off = align256(off + 4 * (size_t)n_planes);
+  L.trig_g = off;     off = align256(off + 16 * (size_t)(F * n_t));
+  L.rot_g = off;      off = align256(off + (size_t)F);
+  L.trig_h = off;     off = align256(off + 16 * (size_t)(max_frames * n_t));
+  L.rot_h = off;      off = align256(off + (size_t)max_frames);
+  L.total = off;
+  return L;
+}
+
+// ------------------------------------------------------------------------------------------ scan kernel params
+struct ScanParams {
+  // score inputs (x0hat == nullptr -> the mask comes from mask_in)
+  const float* x0hat;
+  const float* xref;
+  const uint8_t* mask_in;
+  int32_t n_tok, d;
+  float gamma;
+  int32_t keep_rule;
+  int32_t tile, n_tiles, lpt;  // tokens per tile, tiles, lanes per token of the vector path (0 = warp path)
+  float* ell_out;
+  uint8_t* mask_out;
+  int32_t* idx_out;
+  // control
+  Ctrl* ctrl;
+  unsigned long long* tile_state;
+  int32_t* status;
+  int32_t* kept_dev;
+  int32_t force_timeout;
+  // cache bookkeeping, done by the final CTA
+  int32_t update_cache;   // append kept rows' frames, grow hist_len of dynamic planes
+  int32_t want_rephase;   // list planes whose history must be re-indexed
+  int32_t* hist_len;
+  int32_t* hist_t;
+  const uint8_t* head_is_static;
+  int32_t n_planes;
+  int64_t hist_cap;
+  int32_t evict_first_frame, T;
+  int32_t* dyn_list;
+  int32_t* rp_list;
+  int32_t* rp_len;
+  // phase tables, built by the CTAs numbered past the tiles
+  int32_t n_trig_blocks;
+  float4* trig_g;          // [F][n_t]: turn from t to t~(t; q0) for the leaving chunk's frames
+  uint8_t* rot_g;          // [F]: nonzero if that frame turns at all
+  int32_t g_frames;        // F, or 0 when no gather follows
+  float4* trig_h;          // [max_frames][n_t]: turn from t~(t; q0_prev) to t~(t; q0)
+  uint8_t* rot_h;          // [max_frames]
+  int32_t h_lo, h_hi;      // frames [h_lo, h_hi) of the history table (empty when no re-index follows)
+  int32_t n_t;
+  double base, R, S;
+  int32_t g_mode;
+  int32_t T_s;             // first non-sink frame
+  int32_t q0, q0_prev;
+};
+
+struct GatherParams {
+  char* k;
+  char* v;
+  int64_t plane_bytes;     // cap * row_bytes
+  int32_t row_bytes;       // D * element size (multiple of 16)
+  int32_t vpr;             // 16-byte vectors per row
+  int32_t vpr_shift;       // log2(vpr) when vpr is a power of two, else -1
+  int64_t src_row0;        // first row of the leaving chunk's slot
+  int64_t dst_row0;        // first history row (sink_rows)
+  const Ctrl* ctrl;
+  const int32_t* idx;
+  const int32_t* dyn_list;
+  const float4* trig_g;
+  const uint8_t* rot_g;
+  int32_t T, n_t, dtype;
+  int32_t rows_per_item;
+};
+
+struct RephaseParams {
+  char* k;
+  int64_t plane_bytes;
+  int32_t row_bytes;
+  int32_t nvt;             // 16-byte vectors of a row that hold temporal pairs
+  int64_t hist_row0;       // sink_rows
+  const Ctrl* ctrl;
+  const int32_t* rp_list;
+  const int32_t* rp_len;
+  const int32_t* hist_t;
+  const float4* trig_h;
+  const uint8_t* rot_h;
+  int32_t n_t, dtype;
+  int32_t h_lo, h_hi;      // frames the table covers
+  int32_t* status;
+};
+
+cudaError_t launch_scan(const ScanParams& p, cudaStream_t s);
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t s);
+cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s);
+int sm_count();
+
+// ------------------------------------------------------------------------------------------ device helpers
+#ifdef __CUDACC__
+
+// g and t~ in double with explicit round-to-nearest operations (never contracted into fma), so the decision
+// "does this frame's phase change" is taken on exactly the values the definition gives.
+__device__ __forceinline__ double dev_g(double delta, double delta_max, double R, double S, int mode) {
+  double span_end = mode == 0 ? S : __dadd_rn(R, S);
+  if (delta <= R || delta_max <= span_end) return delta;
+  return __dadd_rn(__ddiv_rn(__dmul_rn(__dsub_rn(delta, R), __dsub_rn(span_end, R)), __dsub_rn(delta_max, R)), R);
+}
+
+__device__ __forceinline__ double dev_phase(double t, double q0, double T_s, double R, double S, int mode) {
+  return __dsub_rn(q0, dev_g(__dsub_rn(q0, t), __dsub_rn(q0, T_s), R, S, mode));
+}
+
+// cos/sin of an angle as unevaluated float pairs (hi + lo, ~48 significant bits): {c_hi, c_lo, s_hi, s_lo}.
+__device__ __forceinline__ float4 dev_trig_entry(double phi) {
+  double s, c;
+  sincos(phi, &s, &c);
+  float chi = __double2float_rn(c), shi = __double2float_rn(s);
+  return make_float4(chi, __double2float_rn(__dsub_rn(c, (double)chi)), shi,
+                     __double2float_rn(__dsub_rn(s, (double)shi)));
+}
+
+// Rotate one pair (a, b) by the angle whose cos/sin pairs are in t:
+//   out_a = a*c - b*s, out_b = a*s + b*c.
+// The rounding error of the b-products is recovered exactly with an fma and the low parts of cos/sin are added,
+// so the result carries ~2^-23 relative error plus ~2^-47 (|a| + |b|) absolute error: rounding it to bf16 gives
+// the correctly rounded value or its neighbour, never further.
+__device__ __forceinline__ void dev_rotate(float a, float b, const float4 t, float& oa, float& ob) {
+  float q0 = __fmul_rn(b, t.z);
+  float e0 = __fmaf_rn(b, t.z, -q0);
+  float r0 = __fmaf_rn(a, t.x, -q0);
+  float k0 = __fmaf_rn(a, t.y, -__fmul_rn(b, t.w));
+  oa = __fadd_rn(r0, __fsub_rn(k0, e0));
+  float q1 = __fmul_rn(b, t.x);
+  float e1 = __fmaf_rn(b, t.x, -q1);
+  float r1 = __fmaf_rn(a, t.z, q1);
+  float k1 = __fmaf_rn(a, t.w, __fmul_rn(b, t.y));
+  ob = __fadd_rn(r1, __fadd_rn(k1, e1));
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Rotate the pairs held in one 16-byte vector.  p0 = index of its first pair; pairs >= n_t are left as stored.
+// trig points at the table row of the key's frame.
+__device__ __forceinline__ uint4 dev_rotate_vec(uint4 x, int dtype, int p0, int n_t, const float4* trig) {
+  if (dtype == DCP_BF16) {
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      int p = p0 + i;
+      if (p < n_t) {
+        float oa, ob;
+        dev_rotate(bf16lo(w[i]), bf16hi(w[i]), trig[p], oa, ob);
+        w[i] = pack_bf16x2(oa, ob);
+      }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    float f[4] = {__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      int p = p0 + i;
+      if (p < n_t) dev_rotate(f[2 * i], f[2 * i + 1], trig[p], f[2 * i], f[2 * i + 1]);
+    }
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace dcp

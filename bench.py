@@ -1,0 +1,424 @@
+"""Benchmark of the DeCoPrune history-KV prune step on GB300 (one JSON line on rank 0).
+
+One step = one full prune step (score + threshold + index scan + fused K/V gather with key re-phase + history
+re-index) of the full-depth eviction workload: 40 layers x 40 KV heads x head_dim 128 bf16 cache (sink chunk, three
+dense window chunks and the leaving chunk resident, ~31 GB with the history region), 6240 tokens per chunk, score rows
+of 64 fp32 values, ~15% of tokens kept.  Inputs are seeded synthetic tensors of that shape, resident in HBM before
+the timed region; L2 (129 MB) is flushed between steps by writing a 256 MB buffer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dcp|reference] [--no-extra]
+
+`value` is the step's algorithmic bytes (what the method must read and write) divided by the device time of the step
+(CUDA events on the launching stream, max over ranks), summed over ranks.  With N > 1 every rank runs its own replica
+of the workload on its own GPU (the step has no exchange: "weak" scaling).  `--impl reference` times the CPU oracle on
+a bounded sample of the same workload (the only other thing this script may run).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "history-KV prune step GB/s (score+scan+gather+RoPE) & % of GB300 HBM peak"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu_index), "-lms", "50"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def mark(self, name):
+        self.marks.append((name, time.time()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        use = inside if len(inside) >= 3 else [r for r in rows if r[0] <= t1]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median([r[1] for r in use])), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------------------------------------ distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def dist_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------ GPU arm
+class FullDepthStep:
+    """Device state of one eviction of a full-size workload, ready to be pruned repeatedly."""
+
+    def __init__(self, w):
+        import torch
+
+        import autoregressive_video_diffusion_gb300 as dcp
+        from synth import workloads as W
+        self.w, self.dcp = w, dcp
+        c, q0_prev, q0 = w.evictions()[-1]
+        self.c, self.q0_prev, self.q0 = c, q0_prev, q0
+        stream = torch.cuda.current_stream().cuda_stream
+        self.cache = dcp.KVCache(w.L, w.H, w.D, w.dtype, w.cap, w.hist_cap)
+        W.fill_device_chunks(self.cache.k.data_ptr(), self.cache.v.data_ptr(), w,
+                             list(range(w.sink_chunks)) + w.resident_window(c), stream)
+        W.fill_device_history_canary(self.cache.k.data_ptr(), self.cache.v.data_ptr(), w, stream)
+        self.cfg = dcp.Config(gamma=w.gamma, keep_rule=0, sink_chunks=w.sink_chunks, window_chunks=w.window_chunks,
+                              tokens_per_frame=w.tokens_per_frame, frames_per_chunk=w.frames_per_chunk,
+                              n_temporal_pairs=w.n_temporal_pairs, rope_base=w.rope_base, g_recent_R=w.R,
+                              g_span_S=w.S, g_mode=w.g_mode, max_frames=w.max_frames)
+        self.ws = dcp.new_workspace(dcp.dcp_workspace_size(self.cache, self.cfg))
+        x0, xr = w.score_inputs(c)
+        self.x0_host = torch.from_numpy(x0).pin_memory()
+        self.xr_host = torch.from_numpy(xr).pin_memory()
+        self.x0 = self.x0_host.cuda()
+        self.xr = self.xr_host.cuda()
+        self.kept = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.kept_host = torch.zeros(1, dtype=torch.int32).pin_memory()
+        self.hist_len0 = self.cache.hist_len.clone()
+        self.hist_t0 = self.cache.hist_t.clone()
+        self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+
+    def restore(self):
+        self.cache.hist_len.copy_(self.hist_len0)
+        self.cache.hist_t.copy_(self.hist_t0)
+
+    def flush_l2(self):
+        self.flush_buf.fill_(1)
+
+    def step(self, x0=None, xr=None, kept_host=None):
+        w = self.w
+        self.dcp.dcp_prune_step(self.cache, self.cfg, self.x0 if x0 is None else x0, self.xr if xr is None else xr,
+                                w.slot_of(self.c), w.first_frame(self.c), self.q0_prev, self.q0, None, self.kept,
+                                kept_host, self.ws)
+
+    def launches_per_step(self):
+        rephase = self.q0_prev != self.q0 and self.w.n_temporal_pairs > 0
+        return 3 if rephase else 2
+
+
+def run_gpu(w, steps: int, warmup: int, world: int, rank: int, local: int, clocks: ClockSampler | None,
+            e2e_steps: int):
+    import torch
+
+    import autoregressive_video_diffusion_gb300 as dcp
+    s = FullDepthStep(w)
+    stream = torch.cuda.current_stream()
+    ev_scan, ev_gather = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_scan.record(stream)
+    ev_gather.record(stream)
+    torch.cuda.synchronize()
+    # warm-up, and a short sustained pre-roll so the clock sampler sees the part under this load
+    for _ in range(warmup):
+        s.restore()
+        s.step()
+    torch.cuda.synchronize()
+    pre_t = time.time()
+    while time.time() - pre_t < 1.0:
+        s.restore()
+        s.flush_l2()
+        s.step()
+        torch.cuda.synchronize()
+    st = dcp.dcp_get_status(s.cache.status)
+    if st != dcp.DCP_OK:
+        raise RuntimeError(f"prune step reported {dcp.dcp_status_string(st)}")
+    k = int(s.kept.item())
+    n_dyn = w.n_planes
+    hist_rows_changed = 0
+    alg_bytes = w.algorithmic_bytes(k, n_dyn, hist_rows_changed)
+    gather_bytes = k * n_dyn * 2 * (w.D * w.esize) * 2
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    scan_ms, gather_ms = [], []
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark("timed_start")
+    t_wall0 = time.time()
+    dcp.dcp_set_phase_events(ev_scan, ev_gather)
+    for i in range(steps):
+        s.restore()
+        s.flush_l2()
+        starts[i].record(stream)
+        s.step()
+        ends[i].record(stream)
+        ends[i].synchronize()
+        scan_ms.append(starts[i].elapsed_time(ev_scan))
+        gather_ms.append(ev_scan.elapsed_time(ev_gather))
+    dcp.dcp_set_phase_events(None, None)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    t_wall1 = time.time()
+    if clocks:
+        clocks.mark("timed_end")
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = float(np.mean(step_ms))
+    ms_max = dist_max(ms, world)
+
+    # end to end through the public API: pinned host score inputs -> device, the step, kept count -> host
+    e2e_ms = []
+    for _ in range(e2e_steps):
+        s.restore()
+        s.flush_l2()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        s.x0.copy_(s.x0_host, non_blocking=True)
+        s.xr.copy_(s.xr_host, non_blocking=True)
+        s.step(kept_host=s.kept_host)
+        b.record(stream)
+        b.synchronize()
+        assert int(s.kept_host.item()) == k
+        e2e_ms.append(a.elapsed_time(b))
+    e2e = float(np.mean(e2e_ms)) if e2e_ms else None
+    e2e_max = dist_max(e2e, world) if e2e is not None else None
+
+    res = dict(k=k, alg_bytes=alg_bytes, gather_bytes=gather_bytes, ms=ms, ms_max=ms_max,
+               ms_median=float(np.median(step_ms)), scan_ms=float(np.mean(scan_ms)),
+               gather_ms=float(np.mean(gather_ms)), e2e_ms=e2e_max, wall=(t_wall0, t_wall1),
+               launches=steps * s.launches_per_step(), h2d=2 * s.x0.numel() * 4, d2h=4)
+    del s
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------------------------------ CPU oracle (baseline)
+class OracleSample:
+    """The CPU oracle's prune step on a bounded sample of the workload: the whole score / threshold / index scan of
+    the chunk plus the gather and re-phase of `n_planes` of its planes (a host cache holding only those planes, with
+    the values they have in the full workload)."""
+
+    def __init__(self, w, n_planes: int):
+        import oracle
+        import synth
+        from oracle import replay
+        from synth import workloads as W
+        self.oracle, self.w = oracle, w
+        self.c, self.q0_prev, self.q0 = w.evictions()[-1]
+        self.planes = list(range(0, w.n_planes, max(1, w.n_planes // n_planes)))[:n_planes]
+        dt = np.uint16 if w.dtype == 0 else np.float32
+        k_arr = np.zeros((1, len(self.planes), w.cap, w.D), dt)
+        v_arr = np.zeros((1, len(self.planes), w.cap, w.D), dt)
+        for cc in list(range(w.sink_chunks)) + w.resident_window(self.c):
+            row0 = W.chunk_row0(w, cc)
+            for i, p in enumerate(self.planes):
+                for arr, what in ((k_arr, W.S_K), (v_arr, W.S_V)):
+                    synth.fill_rows_host(arr[0, i:i + 1], w.dtype, 1, w.cap, row0, w.C, w.D, w.seed,
+                                         W.chunk_stream(cc, what), w.C, p * w.C)
+        self.hc = oracle.HostCache(k_arr, v_arr, np.zeros(len(self.planes), np.int32),
+                                   np.zeros(max(w.hist_cap, 1), np.int32), w.hist_cap)
+        self.x0, self.xr = w.score_inputs(self.c)
+        self.cfg = replay.cfg_of(w)
+        self.k = 0
+
+    def step(self) -> float:
+        """One timed oracle prune step; returns seconds."""
+        w = self.w
+        self.hc.hist_len[:] = 0
+        t0 = time.perf_counter()
+        rc, _, _, idx = self.oracle.prune_step(self.hc, self.cfg, self.x0, self.xr, w.slot_of(self.c),
+                                               w.first_frame(self.c), self.q0_prev, self.q0)
+        sec = time.perf_counter() - t0
+        assert rc == self.oracle.OK
+        self.k = len(idx)
+        return sec
+
+    def bytes_per_step(self) -> int:
+        w = self.w
+        return 2 * w.C * w.d * 4 + self.k * len(self.planes) * 2 * (w.D * w.esize) * 2 + w.C * 5
+
+    def describe(self, reps: int) -> str:
+        return (f"oracle prune step of {self.w.name}: full score/mask/index scan of {self.w.C} tokens + gather and "
+                f"re-phase of {len(self.planes)} of {self.w.n_planes} planes (k={self.k}), {reps} timed step(s), "
+                f"one thread")
+
+
+# ------------------------------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="dcp", choices=["dcp", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the rotated full-depth line and the CPU baseline")
+    ap.add_argument("--oracle-planes", type=int, default=64)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from synth.workloads import FULL, FULL_ROTATED
+    w = FULL
+    world, rank, local = dist_setup() if args.impl == "dcp" else (int(os.environ.get("WORLD_SIZE", "1")),
+                                                                 int(os.environ.get("RANK", "0")), 0)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import __graft_entry__
+        __graft_entry__.build()
+        sample = OracleSample(w, args.oracle_planes)
+        for _ in range(args.warmup):
+            sample.step()
+        secs = [sample.step() for _ in range(args.steps)]
+        value = sample.bytes_per_step() / float(np.mean(secs)) / 1e9
+        desc = sample.describe(args.steps)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(secs)) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": {"workload": w.name, "L": w.L, "H": w.H, "D": w.D,
+                                                "tokens_per_chunk": w.C, "d": w.d},
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    dist_barrier(world)
+    import autoregressive_video_diffusion_gb300  # noqa: F401
+    torch.cuda.set_device(local)
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    res = run_gpu(w, args.steps, args.warmup, world, rank, local, clocks, e2e_steps=max(3, args.steps // 5))
+    if clocks:
+        clocks.stop()
+        clk = clocks.summary(*res["wall"])
+    extra = {}
+    if not args.no_extra:
+        r2 = run_gpu(FULL_ROTATED, max(5, args.steps // 2), args.warmup, world, rank, local, None, e2e_steps=0)
+        extra["full_depth_rotated"] = {
+            "workload": FULL_ROTATED.name, "q0": FULL_ROTATED.evictions()[-1][2], "kept": r2["k"],
+            "us_per_step": r2["ms_max"] * 1e3, "GB_per_s": r2["alg_bytes"] / (r2["ms_max"] * 1e-3) / 1e9,
+            "gather_us": r2["gather_ms"] * 1e3,
+            "gather_GB_per_s": r2["gather_bytes"] / (r2["gather_ms"] * 1e-3) / 1e9}
+    if rank != 0:
+        return
+    peak, peak_kind = _peaks()
+    value = world * res["alg_bytes"] / (res["ms_max"] * 1e-3) / 1e9
+    gather_gbs = res["gather_bytes"] / (res["gather_ms"] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_max"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "L": w.L, "H": w.H, "D": w.D, "tokens_per_chunk": w.C, "d": w.d,
+                   "kept": res["k"], "evicting_chunk": w.evictions()[-1][0], "q0": w.evictions()[-1][2],
+                   "algorithmic_bytes_per_step": res["alg_bytes"], "l2": "flushed between steps (256 MB write)",
+                   "compute": "fp32 score, fp32 compensated rotation, bf16 storage"},
+        "us_per_step": res["ms_max"] * 1e3,
+        "pct_of_nominal_hbm": 100.0 * (value / world) / NOMINAL_HBM_GBS,
+        "pct_of_measured_hbm": 100.0 * (value / world) / peak,
+        "roofline": {"bound": "hbm", "kernel": "gather_kernel", "achieved": gather_gbs, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": gather_gbs / peak, "traffic": None},
+        "phases_us": {"scan": res["scan_ms"] * 1e3, "gather": res["gather_ms"] * 1e3},
+        "gpu_launches": res["launches"],
+        "clocks": clk,
+    }
+    if res["e2e_ms"] is not None:
+        line["e2e"] = {"value": world * res["alg_bytes"] / (res["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                       "us_per_step": res["e2e_ms"] * 1e3}
+    if extra:
+        line["extra"] = extra
+    if not args.no_extra:
+        sample = OracleSample(w, args.oracle_planes)
+        sample.step()
+        secs = [sample.step() for _ in range(5)]
+        line["cpu_baseline"] = {"value": sample.bytes_per_step() / float(np.mean(secs)) / 1e9, "unit": "GB/s",
+                                "cores": 1, "kind": "oracle", "sample": sample.describe(5),
+                                "host_cores_available": cores}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/* dcp.h - C ABI of the GB300 DeCoPrune history-KV prune step (libdcp.so).
+ *
+ * The method is the one described on the page "DeCoPrune이 디노이징 불일치로 비디오 KV 캐시를 85% 줄인다"
+ * (onedev.kr/papers/726).  Sections of that page are cited as:
+ *   [how]     어떻게 동작하나 "how it works":   per-token discrepancy l = (1/d)||x0hat(tau*) - x_final||^2, threshold
+ *                                             gamma into one binary mask shared by all layers, protected sink chunk,
+ *                                             dense window of the w most recent chunks, physical gather K[m], V[m]
+ *                                             when a non-sink chunk leaves the window.
+ *   [differs] 무엇과 다른가 "what differs":   prefix pruning (score the re-noised observed chunk against the clean
+ *                                             one), RoPE re-indexing t~(t) = q0 - g(q0 - t) of key phase only, and
+ *                                             the head-specialised variant (static heads: Streaming; dynamic heads:
+ *                                             DeCoPrune).
+ *   [use]     어떻게 쓰나 "how to use":        cumulative history-KV position reduction (PR) versus FullKV.
+ *   [limits]  전제와 한계:                      schedule (999, 957, 899, 702), probe index 2 (tau* = 899), gamma 0.10.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named *_dev, and every pointer inside dcp_cache, are DEVICE pointers owned by the caller.  Pointers
+ *     named *_host are host pointers.  The library never allocates, frees or keeps any pointer past the call.
+ *   - `stream` is a cudaStream_t passed as void*.  Every call is asynchronous on that stream.
+ *   - Host-detectable errors (null or misaligned pointers, bad sizes, bad config) return before any launch and
+ *     change nothing.  Errors only the device can see (history capacity exceeded, inconsistent head lengths, a
+ *     bounded wait that gave up) are written to the cache's (or the caller's) device status word; nothing traps.
+ *     Read it with dcp_get_status().  A step that sets a device error leaves the cache contents and lengths as
+ *     they were.
+ *   - The workspace is caller-owned device scratch of dcp_workspace_size() bytes, 256-byte aligned.  Zero it once
+ *     with dcp_workspace_init() before its first use; every call leaves it ready for the next.  Calls that share a
+ *     workspace or a cache must be ordered on one stream (not thread-safe per workspace or cache).
+ *
+ * KV cache layout (dcp_cache): K and V are [L][H][cap][D] arrays (bf16 or fp32), row-major, one plane of cap rows
+ * per (layer, head).  Rows of a plane are laid out as
+ *     [0, sink_rows)                       sink chunks (sink_chunks * C rows), never touched
+ *     [sink_rows, sink_rows + hist_cap)    compacted history; hist_len[l*H + h] rows are valid
+ *     [sink_rows + hist_cap, cap)          dense window ring of (window_chunks + 1) slots of C rows
+ * with C = tokens_per_frame * frames_per_chunk.  Token n of a chunk (frame-major, then raster order inside a
+ * frame) is row n of its slot and row n of the score inputs; its latent frame is first_frame + n / tokens_per_frame.
+ * hist_t[j] is the latent frame of history position j; it is shared by every plane (all dynamic heads keep the same
+ * tokens because the mask is shared; static heads keep none).  Keys are stored rotated (RoPE): the first
+ * n_temporal_pairs pairs (2p, 2p+1) carry the temporal coordinate with frequency theta_p = rope_base^(-p / n_t).
+ */
+#ifndef DCP_H
+#define DCP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t dcp_status;
+#define DCP_OK 0
+#define DCP_EINVAL 1    /* invalid argument, detected on the host before any launch */
+#define DCP_ECAPACITY 2 /* device: history would exceed hist_cap; the step was skipped */
+#define DCP_ECUDA 3     /* a CUDA runtime call failed */
+#define DCP_ETIMEOUT 4  /* device: a bounded wait of the index scan gave up; outputs of that call are invalid */
+#define DCP_EDEVICE 5   /* device: dynamic heads disagree on hist_len (corrupt cache state); the step was skipped */
+
+#define DCP_BF16 0
+#define DCP_F32 1
+
+typedef struct dcp_cache {
+  void* k;            /* device [L][H][cap][D], 16-byte aligned; D * element size must be a multiple of 16 */
+  void* v;            /* device, same shape and type as k */
+  int32_t L, H, D;    /* layers, KV heads, head_dim (D even) */
+  int32_t dtype;      /* DCP_BF16 or DCP_F32 */
+  int64_t cap;        /* rows per plane, >= sink_rows + hist_cap + (window_chunks + 1) * C */
+  int64_t hist_cap;   /* history rows per plane */
+  int32_t* hist_len;  /* device [L*H], in/out */
+  int32_t* hist_t;    /* device [hist_cap], in/out */
+  int32_t* status;    /* device, one int32: first device-side error of a call (0 = none) */
+} dcp_cache;
+
+typedef struct dcp_config {
+  float gamma;               /* threshold on l; the page's value is 0.10 [limits] */
+  int32_t keep_rule;         /* 0: keep l > gamma (DeCoPrune [how]); 1: the reverse criterion, keep !(l > gamma) */
+  int32_t sink_chunks;       /* protected leading chunks [how] */
+  int32_t window_chunks;     /* w: most recent chunks kept dense [how] */
+  int32_t tokens_per_frame;  /* T latent tokens per latent frame */
+  int32_t frames_per_chunk;  /* F latent frames per chunk (4 on the page [limits]) */
+  int32_t n_temporal_pairs;  /* n_t leading rotary pairs that carry the temporal coordinate (0 <= n_t <= D/2) */
+  int32_t pair_layout;       /* 0: pair p occupies dims (2p, 2p+1); no other layout is supported */
+  double rope_base;          /* rotary base of the temporal ladder */
+  double g_recent_R;         /* g is the identity on offsets <= R; must satisfy R >= window_chunks * F */
+  double g_span_S;           /* g_mode 0: total virtual span (oldest history offset maps to S, S >= R);
+                                g_mode 1: old offsets are compressed into (R, R + S] */
+  int32_t g_mode;
+  int32_t rephase_sink;      /* must be 0: the sink keeps its stored phase */
+  int32_t max_frames;        /* largest q0 (latent frame index) the workspace is sized for */
+  int32_t reserved;          /* must be 0 */
+} dcp_config;
+
+/* Bytes of device workspace the cache/config need (prune, compact, re-index and score calls for this cache). */
+size_t dcp_workspace_size(const dcp_cache* cache, const dcp_config* cfg);
+
+/* Bytes of device workspace a standalone dcp_score_mask over n_tok tokens needs. */
+size_t dcp_score_workspace_size(int32_t n_tok);
+
+/* Zero a workspace (stream-ordered).  Needed once per workspace, before its first use. */
+dcp_status dcp_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* Score + threshold + ordered index list for one chunk [how], [differs: prefix pruning uses xref = clean chunk].
+ *   x0hat_dev, xref_dev : fp32 [n_tok][d] row-major (the probe-step clean prediction and the final output, or the
+ *                         re-noised prediction and the clean observed chunk in the prefix pass).
+ *   ell_dev   (nullable): fp32 [n_tok] out, l[n] = (1/d) sum_j (x0hat[n][j] - xref[n][j])^2, fp32 arithmetic.
+ *   mask_dev  (nullable): uint8 [n_tok] out, 1 = keep (rule from keep_rule).
+ *   idx_dev   (nullable): int32 [n_tok] out, increasing kept positions in [0, kept).
+ *   kept_dev  (nullable): int32 out, number of kept tokens.
+ *   status_dev          : int32 device status word (DCP_ETIMEOUT if a bounded wait gave up).
+ * Errors: DCP_EINVAL for null inputs, n_tok < 1 or > 2^30, d < 1, non-finite gamma, short workspace. */
+dcp_status dcp_score_mask(const float* x0hat_dev, const float* xref_dev, int32_t n_tok, int32_t d, float gamma,
+                          int32_t keep_rule, float* ell_dev, uint8_t* mask_dev, int32_t* idx_dev, int32_t* kept_dev,
+                          int32_t* status_dev, void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* Physical compaction of the leaving chunk [how] with the fused key re-phase [differs].
+ * The chunk in ring slot evict_slot (its first latent frame is evict_first_frame) is compacted: for every
+ * dynamic plane, K and V rows idx[j] of the slot (the kept positions of mask_dev, uint8 [C]) are appended in order
+ * at hist_len; each appended key's temporal pairs turn from its stored frame t to t~(t; q0); values and every other
+ * key dim are copied bitwise.  hist_len of dynamic planes grows by kept, hist_t gets the kept frames.  Planes with
+ * head_is_static_dev[l*H+h] != 0 (nullable: none) follow the Streaming policy and keep nothing.  The ring slot is
+ * left as it was.  kept_dev (nullable) receives the kept count.
+ * Device errors: DCP_ECAPACITY (hist_len + kept > hist_cap), DCP_EDEVICE (dynamic planes disagree on hist_len).
+ * Host errors: DCP_EINVAL (see dcp_cache/dcp_config; evict_slot outside [0, w]; evict_first_frame < sink frames;
+ * q0 < evict_first_frame + F; q0 > max_frames). */
+dcp_status dcp_compact_layers(const dcp_cache* cache, const dcp_config* cfg, int32_t evict_slot,
+                              int32_t evict_first_frame, const uint8_t* mask_dev, const uint8_t* head_is_static_dev,
+                              int32_t q0, int32_t* kept_dev, void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* RoPE re-index of the history already present [differs]: when the query frame moves from q0_prev to q0, every
+ * history key whose t~(t) changes turns its temporal pairs by theta_p * (t~(t; q0) - t~(t; q0_prev)) in place.
+ * Rows whose t~ does not change are not touched.  Values are never touched.
+ * Host errors: DCP_EINVAL (q0_prev > q0, q0 > max_frames, q0_prev < sink frames, bad cache/config). */
+dcp_status dcp_rope_reindex(const dcp_cache* cache, const dcp_config* cfg, int32_t q0_prev, int32_t q0,
+                            void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* One full prune step, the unit the library is measured on: score the leaving chunk (x0hat/xref fp32 [C][d]),
+ * threshold it, build the index list, re-index the history present before the step from q0_prev to q0, and compact
+ * the chunk into the history with its keys re-phased to q0.  Equivalent to dcp_score_mask + dcp_rope_reindex +
+ * dcp_compact_layers on the same arguments.  kept_dev (nullable, device) and kept_host_pinned (nullable, pinned
+ * host memory, written by a stream-ordered copy) receive the kept count.  dcp_workspace_outputs() gives the device
+ * addresses where the step leaves l, the mask and the index list. */
+dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const float* x0hat_dev, const float* xref_dev,
+                          int32_t d, int32_t evict_slot, int32_t evict_first_frame, int32_t q0_prev, int32_t q0,
+                          const uint8_t* head_is_static_dev, int32_t* kept_dev, int32_t* kept_host_pinned,
+                          void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* Device addresses inside a prune-step workspace: l (fp32 [C]), the mask (uint8 [C]) and the index list
+ * (int32 [C], first `kept` entries valid) of the last dcp_prune_step / dcp_compact_layers call. */
+dcp_status dcp_workspace_outputs(const dcp_cache* cache, const dcp_config* cfg, void* workspace_dev, float** ell_dev,
+                                 uint8_t** mask_dev, int32_t** idx_dev);
+
+/* Synchronise `stream` and return the device status word (DCP_OK if no device error was recorded). */
+dcp_status dcp_get_status(const int32_t* status_dev, void* stream);
+
+/* Clear the device status word (stream-ordered). */
+dcp_status dcp_reset_status(int32_t* status_dev, void* stream);
+
+const char* dcp_status_string(dcp_status s);
+
+/* Cumulative PR bookkeeping [use]: PR = 1 - visible / full summed over generated chunks, where a chunk that has
+ * `prior_tokens` tokens before it sees, in each of n_planes planes, the sink, its hist_len rows and the dense
+ * window; FullKV would see all prior tokens.  hist_len_sum is the sum of hist_len over the planes (host value). */
+typedef struct dcp_pr_counter {
+  int64_t visible;
+  int64_t full;
+} dcp_pr_counter;
+void dcp_pr_add_chunk(dcp_pr_counter* acc, int64_t n_planes, int64_t hist_len_sum, int64_t sink_tokens_visible,
+                      int64_t window_tokens_visible, int64_t prior_tokens);
+double dcp_pr_value(const dcp_pr_counter* acc);
+
+/* Profiling hook.  When ev_after_scan / ev_after_gather are non-null (cudaEvent_t passed as void*), every later
+ * dcp_prune_step records them on its stream right after the scan kernel and right after the gather kernel, so a
+ * caller can time each kernel with CUDA events inside a timed region.  Pass nulls to switch it off.  Process-wide
+ * setting, not thread-safe. */
+dcp_status dcp_set_phase_events(void* ev_after_scan, void* ev_after_gather);
+
+/* ABI check for bindings: (sizeof(dcp_cache) << 16) | sizeof(dcp_config). */
+uint32_t dcp_abi_struct_sizes(void);
+
+/* Test hook: when on != 0, index-scan tiles stop publishing their counts, so every later tile's bounded wait runs
+ * out and the call reports DCP_ETIMEOUT (no hang, no trap).  Returns the previous setting. */
+int32_t dcp_debug_force_scan_timeout(int32_t on);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCP_H */

@@ -234,3 +234,53 @@ def scaled(w: Workload, **over) -> Workload:
     """A copy of workload w with some fields replaced (smaller parity cases of the same recipe)."""
     import dataclasses
     return dataclasses.replace(w, **over)
+
+
+def chunk_row0(w: Workload, c: int) -> int:
+    """First cache row of chunk c: the sink rows for sink chunks, else its ring slot."""
+    return c * w.C if c < w.sink_chunks else w.win_row0 + w.slot_of(c) * w.C
+
+
+def fill_device_chunks(k_ptr: int, v_ptr: int, w: Workload, chunks, cuda_stream: int, planes=None) -> None:
+    """Write the seeded K and V of each chunk in `chunks` into its rows of a device cache [L][H][cap][D].
+
+    `planes` (optional list of original plane indices) fills a cache that holds only those planes, in that order,
+    with the values they have in the full workload."""
+    from . import fill_rows_device
+    for c in chunks:
+        row0 = chunk_row0(w, c)
+        for ptr, what in ((k_ptr, S_K), (v_ptr, S_V)):
+            if planes is None:
+                fill_rows_device(ptr, w.dtype, w.n_planes, w.cap, row0, w.C, w.D, w.seed, chunk_stream(c, what),
+                                 w.C, 0, cuda_stream)
+            else:
+                for i, p in enumerate(planes):
+                    fill_rows_device(ptr + i * w.cap * w.D * w.esize, w.dtype, 1, w.cap, row0, w.C, w.D, w.seed,
+                                     chunk_stream(c, what), w.C, p * w.C, cuda_stream)
+
+
+def fill_device_history_canary(k_ptr: int, v_ptr: int, w: Workload, cuda_stream: int, planes=None) -> None:
+    """Seeded contents of the (not yet used) history rows, so stray writes show up."""
+    from . import fill_rows_device
+    if not w.hist_cap:
+        return
+    for ptr, s in ((k_ptr, 2 * STREAM_HIST_INIT), (v_ptr, 2 * STREAM_HIST_INIT + 1)):
+        if planes is None:
+            fill_rows_device(ptr, w.dtype, w.n_planes, w.cap, w.sink_rows, w.hist_cap, w.D, w.seed, s, w.hist_cap, 0,
+                             cuda_stream)
+        else:
+            for i, p in enumerate(planes):
+                fill_rows_device(ptr + i * w.cap * w.D * w.esize, w.dtype, 1, w.cap, w.sink_rows, w.hist_cap, w.D,
+                                 w.seed, s, w.hist_cap, p * w.hist_cap, cuda_stream)
+
+
+def host_chunk_rows(w: Workload, c: int, plane: int, what: int, rows) -> np.ndarray:
+    """Host copy of rows `rows` (positions inside chunk c) of one plane's K (what=S_K) or V (S_V)."""
+    from . import fill_rows_host
+    dt = np.uint16 if w.dtype == 0 else np.float32
+    out = np.empty((len(rows), w.D), dt)
+    tmp = np.empty((1, w.D), dt)
+    for i, r in enumerate(rows):
+        fill_rows_host(tmp, w.dtype, 1, 1, 0, 1, w.D, w.seed, chunk_stream(c, what), w.C, plane * w.C + int(r))
+        out[i] = tmp[0]
+    return out

@@ -11,18 +11,9 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the libdcp kernels)")
     config.addinivalue_line("markers", "slow: long-running case")
-
-
-@pytest.fixture(scope="session", autouse=True)
-def _built():
-    import oracle
-    import synth
-    oracle.build()
-    synth.build()
-    if os.path.exists(os.path.join(ROOT, "__graft_entry__.py")):
-        import __graft_entry__
-        __graft_entry__.build()
-    yield
+    # test modules import the libraries at collection time, so build them (if stale) before collecting
+    import __graft_entry__
+    __graft_entry__.build()
 
 
 def has_gpu() -> bool:
