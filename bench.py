@@ -104,24 +104,36 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------ distributed
-def dist_setup():
+_BACKEND = {"name": None}
+
+
+def dist_setup(backend: str | None = None):
+    """Join the process group the launcher set up (RANK / WORLD_SIZE / LOCAL_RANK / MASTER_*).  NCCL on GPUs; gloo
+    for the CPU tests of this logic.  Returns (world, rank, local_rank)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        backend = backend or "nccl"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+        _BACKEND["name"] = backend
     return world, rank, local
 
 
 def dist_max(x: float, world: int) -> float:
+    """Max of x over the ranks (the step time the whole job waited for)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if _BACKEND["name"] == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -130,6 +142,11 @@ def dist_barrier(world: int):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def job_throughput(bytes_per_rank_step: int, ms_max: float, world: int) -> float:
+    """Whole-job GB/s: every rank moves its own replica's bytes; the job waits for the slowest rank."""
+    return world * bytes_per_rank_step / (ms_max * 1e-3) / 1e9
 
 
 # ------------------------------------------------------------------------------------------ GPU arm
@@ -385,7 +402,7 @@ def main():
     if rank != 0:
         return
     peak, peak_kind = _peaks()
-    value = world * res["alg_bytes"] / (res["ms_max"] * 1e-3) / 1e9
+    value = job_throughput(res["alg_bytes"], res["ms_max"], world)
     gather_gbs = res["gather_bytes"] / (res["gather_ms"] * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -405,7 +422,7 @@ def main():
         "clocks": clk,
     }
     if res["e2e_ms"] is not None:
-        line["e2e"] = {"value": world * res["alg_bytes"] / (res["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+        line["e2e"] = {"value": job_throughput(res["alg_bytes"], res["e2e_ms"], world), "unit": "GB/s",
                        "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                        "us_per_step": res["e2e_ms"] * 1e3}
     if extra:

@@ -434,5 +434,14 @@ def test_rollout_gpu_trajectory(gpu):
     nt2 = 2 * w.n_temporal_pairs
     assert np.array_equal(g.k[..., nt2:], hc.k[..., nt2:])
     d = replay.ulp_distance(g.k[..., :nt2], hc.k[..., :nt2])
-    print(f"rollout drift: max {int(d.max())} ulp, {int(np.count_nonzero(d))} of {d.size} entries differ")
-    assert int(d.max()) <= 3
+    # A one-ulp difference in the large component of a pair turns, at the next re-index, into an error of the same
+    # absolute size in the other component, which can be many of its own ulps when that component is near zero.
+    # So drift is bounded relative to the pair's length: at most one bf16 rounding (2^-8) per step.
+    gf = synth.bf16_bits_to_f32(g.k[..., :nt2]).astype(np.float64).reshape(-1, w.n_temporal_pairs, 2)
+    of = synth.bf16_bits_to_f32(hc.k[..., :nt2]).astype(np.float64).reshape(-1, w.n_temporal_pairs, 2)
+    rel = np.abs(gf - of).max(axis=2) / np.maximum(np.hypot(of[..., 0], of[..., 1]), 1e-30)
+    steps = len(w.evictions())
+    print(f"rollout drift over {steps} steps: {int(np.count_nonzero(d))} of {d.size} entries differ, max "
+          f"{int(d.max())} ulp of the entry, max {rel.max():.3g} of the pair length")
+    assert rel.max() <= steps * 2.0 ** -8
+    assert np.count_nonzero(d) <= 1e-4 * d.size
