@@ -75,6 +75,7 @@ _SIGS = {
     "dcp_pr_value": ([ctypes.POINTER(DcpPrCounter)], ctypes.c_double),
     "dcp_abi_struct_sizes": ([], ctypes.c_uint32),
     "dcp_set_phase_events": ([_vp, _vp], _i32),
+    "dcp_prune_step_noalloc": ([_pc, _pg, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
     "dcp_debug_force_scan_timeout": ([_i32], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -213,6 +214,21 @@ def dcp_prune_step(cache: KVCache, cfg: Config, x0hat: torch.Tensor, xref: torch
     _check(lib.dcp_prune_step(ctypes.byref(cc), ctypes.byref(gc), _ptr(x0hat), _ptr(xref), x0hat.shape[1],
                               evict_slot, evict_first_frame, q0_prev, q0, _ptr(head_is_static), _ptr(kept_dev),
                               _ptr(kept_host_pinned), _ptr(ws), ws.numel(), _stream(stream)), "dcp_prune_step")
+
+
+DCP_NOALLOC_WORKSPACE_BYTES = 4 << 20
+
+
+def dcp_prune_step_noalloc(cache: KVCache, cfg: Config, x0hat: torch.Tensor, xref: torch.Tensor, evict_slot: int,
+                           evict_first_frame: int, q0_prev: int, q0: int, head_is_static, kept_dev, kept_host_pinned,
+                           stream=None) -> None:
+    """dcp_prune_step without a workspace, for callers that cannot allocate device memory: the library's own fixed
+    scratch array (DCP_NOALLOC_WORKSPACE_BYTES per GPU) is used instead.  Calls that overlap on the GPU race."""
+    cc, gc = cache.c(), cfg.c()
+    _check(lib.dcp_prune_step_noalloc(ctypes.byref(cc), ctypes.byref(gc), _ptr(x0hat), _ptr(xref), x0hat.shape[1],
+                                      evict_slot, evict_first_frame, q0_prev, q0, _ptr(head_is_static),
+                                      _ptr(kept_dev), _ptr(kept_host_pinned), _stream(stream)),
+           "dcp_prune_step_noalloc")
 
 
 def dcp_workspace_outputs(cache: KVCache, cfg: Config, ws: torch.Tensor):

@@ -143,6 +143,27 @@ dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const f
                           const uint8_t* head_is_static_dev, int32_t* kept_dev, int32_t* kept_host_pinned,
                           void* workspace_dev, size_t ws_bytes, void* stream);
 
+/* Largest workspace dcp_prune_step_noalloc can use: 4 MiB (the full-depth 40 x 40 x 128 cache with 6240-token
+ * chunks and max_frames 256 needs about 190 KB). */
+#define DCP_NOALLOC_WORKSPACE_BYTES (4u << 20)
+
+/* dcp_prune_step for callers that cannot allocate device memory (for example code running inside a device
+ * allocator's callback, or an engine that forbids allocation after start-up).  The paper has no counterpart: this
+ * is a packaging variant of dcp_prune_step, with the same arguments minus the workspace and the same results.
+ * Instead of a caller workspace it uses a scratch array of DCP_NOALLOC_WORKSPACE_BYTES compiled into the library,
+ * which every GPU that loads the library holds until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *   - Returns DCP_EINVAL when dcp_workspace_size(cache, cfg) is 0 (invalid) or larger than the scratch array, and
+ *     for every argument dcp_prune_step rejects.
+ *   - The first call made with a given device current looks up the array's device address (cudaGetSymbolAddress)
+ *     for that device; make that first call before any stream capture.
+ *   - Every call shares the one array.  The parts that must start at zero are cleared on `stream` at the start of
+ *     each call; calls whose work overlaps on the GPU (other streams or threads on the same device) race on it. */
+dcp_status dcp_prune_step_noalloc(const dcp_cache* cache, const dcp_config* cfg, const float* x0hat_dev,
+                                  const float* xref_dev, int32_t d, int32_t evict_slot, int32_t evict_first_frame,
+                                  int32_t q0_prev, int32_t q0, const uint8_t* head_is_static_dev, int32_t* kept_dev,
+                                  int32_t* kept_host_pinned, void* stream);
+
 /* Device addresses inside a prune-step workspace: l (fp32 [C]), the mask (uint8 [C]) and the index list
  * (int32 [C], first `kept` entries valid) of the last dcp_prune_step / dcp_compact_layers call. */
 dcp_status dcp_workspace_outputs(const dcp_cache* cache, const dcp_config* cfg, void* workspace_dev, float** ell_dev,
