@@ -28,7 +28,7 @@ dcp_status check_cache_cfg(const dcp_cache* c, const dcp_config* g, Derived* d) 
   if (c->L < 1 || c->H < 1 || c->D < 2 || (c->D & 1)) return DCP_EINVAL;
   if (c->dtype != DCP_BF16 && c->dtype != DCP_F32) return DCP_EINVAL;
   const int es = c->dtype == DCP_BF16 ? 2 : 4;
-  if (((int64_t)c->D * es) % 16) return DCP_EINVAL;
+  if (((int64_t)c->D * es) % 16 || (int64_t)c->D * es > 16384) return DCP_EINVAL;
   if (!aligned(c->k, 16) || !aligned(c->v, 16) || !aligned(c->hist_len, 4) || !aligned(c->hist_t, 4) ||
       !aligned(c->status, 4))
     return DCP_EINVAL;
@@ -107,13 +107,9 @@ ScanParams cache_scan_params(const dcp_cache* c, const dcp_config* g, const Deri
   sp.status = c->status;
   sp.force_timeout = g_force_timeout;
   sp.hist_len = c->hist_len;
-  sp.hist_t = c->hist_t;
   sp.n_planes = (int32_t)d.n_planes;
+  sp.n_plane_slices = (int32_t)((d.n_planes + kThreads - 1) / kThreads);
   sp.hist_cap = c->hist_cap;
-  sp.T = g->tokens_per_frame;
-  sp.dyn_list = at<int32_t>(ws, d.lay.dyn_list);
-  sp.rp_list = at<int32_t>(ws, d.lay.rp_list);
-  sp.rp_len = at<int32_t>(ws, d.lay.rp_len);
   sp.trig_g = at<float4>(ws, d.lay.trig_g);
   sp.rot_g = at<uint8_t>(ws, d.lay.rot_g);
   sp.trig_h = at<float4>(ws, d.lay.trig_h);
@@ -129,30 +125,31 @@ ScanParams cache_scan_params(const dcp_cache* c, const dcp_config* g, const Deri
 
 void finish_tables(ScanParams& sp) {
   const int entries = (sp.g_frames + (sp.h_hi - sp.h_lo)) * sp.n_t;
-  sp.n_trig_blocks = (entries + kThreads - 1) / kThreads;
+  sp.n_trig_blocks = (entries + kTableEntries - 1) / kTableEntries;
 }
 
-GatherParams gather_params(const dcp_cache* c, const dcp_config* g, const Derived& d, void* ws, int32_t slot) {
+GatherParams gather_params(const dcp_cache* c, const dcp_config* g, const Derived& d, void* ws, int32_t slot,
+                           const uint8_t* head_is_static, int32_t evict_first_frame) {
   GatherParams gp{};
   gp.k = static_cast<char*>(c->k);
   gp.v = static_cast<char*>(c->v);
   gp.row_bytes = c->D * d.esize;
   gp.plane_bytes = c->cap * (int64_t)gp.row_bytes;
   gp.vpr = gp.row_bytes / 16;
-  gp.vpr_shift = -1;
-  for (int s = 0; s < 31; ++s)
-    if ((1 << s) == gp.vpr) gp.vpr_shift = s;
   gp.src_row0 = d.win_row0 + (int64_t)slot * d.C;
   gp.dst_row0 = d.sink_rows;
+  gp.n_planes = (int32_t)d.n_planes;
   gp.ctrl = at<Ctrl>(ws, 0);
   gp.idx = at<int32_t>(ws, d.lay.idx);
-  gp.dyn_list = at<int32_t>(ws, d.lay.dyn_list);
+  gp.head_is_static = head_is_static;
+  gp.hist_len = c->hist_len;
+  gp.hist_t = c->hist_t;
+  gp.evict_first_frame = evict_first_frame;
   gp.trig_g = at<float4>(ws, d.lay.trig_g);
   gp.rot_g = at<uint8_t>(ws, d.lay.rot_g);
   gp.T = g->tokens_per_frame;
   gp.n_t = g->n_temporal_pairs;
   gp.dtype = c->dtype;
-  gp.rows_per_item = 16384 / gp.row_bytes > 0 ? 16384 / gp.row_bytes : 1;
   return gp;
 }
 
@@ -164,9 +161,9 @@ RephaseParams rephase_params(const dcp_cache* c, const dcp_config* g, const Deri
   rp.plane_bytes = c->cap * (int64_t)rp.row_bytes;
   rp.nvt = (2 * g->n_temporal_pairs * d.esize + 15) / 16;
   rp.hist_row0 = d.sink_rows;
+  rp.n_planes = (int32_t)d.n_planes;
   rp.ctrl = at<Ctrl>(ws, 0);
-  rp.rp_list = at<int32_t>(ws, d.lay.rp_list);
-  rp.rp_len = at<int32_t>(ws, d.lay.rp_len);
+  rp.hist_len = c->hist_len;
   rp.hist_t = c->hist_t;
   rp.trig_h = at<float4>(ws, d.lay.trig_h);
   rp.rot_h = at<uint8_t>(ws, d.lay.rot_h);
@@ -271,7 +268,8 @@ dcp_status dcp_compact_layers(const dcp_cache* cache, const dcp_config* cfg, int
   finish_tables(sp);
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
-  return cuda_ok(launch_gather(gather_params(cache, cfg, d, ws, evict_slot), st));
+  return cuda_ok(
+      launch_gather(gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame), st, true));
 }
 
 dcp_status dcp_rope_reindex(const dcp_cache* cache, const dcp_config* cfg, int32_t q0_prev, int32_t q0, void* ws,
@@ -291,7 +289,7 @@ dcp_status dcp_rope_reindex(const dcp_cache* cache, const dcp_config* cfg, int32
   finish_tables(sp);
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
-  return cuda_ok(launch_rephase(rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi), st));
+  return cuda_ok(launch_rephase(rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi), st, true));
 }
 
 dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const float* x0hat, const float* xref,
@@ -328,16 +326,18 @@ dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const f
   sp.q0 = q0;
   sp.q0_prev = q0_prev;
   finish_tables(sp);
+  // scan -> re-index (reads the history lengths before the step) -> gather (grows them)
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
-  if (g_ev_after_scan && cudaEventRecord(g_ev_after_scan, st) != cudaSuccess) return DCP_ECUDA;
-  rc = cuda_ok(launch_gather(gather_params(cache, cfg, d, ws, evict_slot), st));
-  if (rc != DCP_OK) return rc;
-  if (g_ev_after_gather && cudaEventRecord(g_ev_after_gather, st) != cudaSuccess) return DCP_ECUDA;
   if (rephase) {
-    rc = cuda_ok(launch_rephase(rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi), st));
+    rc = cuda_ok(launch_rephase(rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi), st, true));
     if (rc != DCP_OK) return rc;
   }
+  if (g_ev_after_scan && cudaEventRecord(g_ev_after_scan, st) != cudaSuccess) return DCP_ECUDA;
+  rc = cuda_ok(launch_gather(gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame), st,
+                             g_ev_after_scan == nullptr));
+  if (rc != DCP_OK) return rc;
+  if (g_ev_after_gather && cudaEventRecord(g_ev_after_gather, st) != cudaSuccess) return DCP_ECUDA;
   if (kept_host_pinned)
     rc = cuda_ok(cudaMemcpyAsync(kept_host_pinned, &at<Ctrl>(ws, 0)->k, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
   return rc;

@@ -17,30 +17,38 @@ constexpr uint32_t kFlagPrefix = 2u;   // tile published its inclusive prefix
 constexpr int kSpinLimit = 1 << 22;    // bounded look-back wait (x ~64 ns backoff -> well under a second)
 constexpr int kForcedSpinLimit = 4096;
 
-// Control block at the start of the workspace.  Fields written by the scan kernel's final CTA are read by the
-// gather and re-index kernels that follow it on the stream.
+// Control block at the start of the workspace.  The scan kernel's final CTA writes the verdict fields, which the
+// re-index and gather kernels that follow it on the stream read.  Counters and accumulators start at zero (a zeroed
+// workspace) and the final CTA puts them back to zero at the end of every call.
 struct Ctrl {
-  uint32_t ticket;      // dynamic CTA numbering of the scan kernel (reset to 0 at the end of every call)
-  uint32_t done;        // CTAs of the scan kernel that finished (reset to 0 at the end of every call)
-  int32_t tile_error;   // a tile's bounded wait gave up during this call (reset by the final CTA)
-  int32_t abort;        // final verdict of the scan kernel: nonzero -> later kernels of the call do nothing
-  int32_t k;            // kept tokens
-  int32_t n_dyn;        // planes that receive the kept rows
-  int32_t common_len;   // their history length before the step
-  int32_t n_rp;         // planes with history rows to re-index
-  int32_t rp_max;       // longest such history
-  int32_t pad[55];
+  uint32_t ticket;          // dynamic CTA numbering of the scan kernel
+  uint32_t done;            // CTAs of the scan kernel that finished
+  int32_t tile_error;       // a tile's bounded wait gave up during this call
+  int32_t abort;            // verdict: nonzero -> the later kernels of the call do nothing
+  int32_t k;                // kept tokens
+  int32_t has_dyn;          // at least one plane receives the kept rows
+  int32_t common_len;       // history length of the receiving planes before the step
+  int32_t first_dyn;        // lowest receiving plane (its gather items also append hist_t), -1 if none
+  int32_t rp_max;           // longest history of any plane before the step (re-index extent)
+  // plane checks, accumulated with atomicMax by the scan CTAs (0 = nothing seen yet)
+  int32_t acc_len_max1;     // max over receiving planes of hist_len + 1
+  int32_t acc_len_min_inv;  // max over receiving planes of INT32_MAX - hist_len
+  int32_t acc_first_inv;    // max over receiving planes of INT32_MAX - plane
+  int32_t acc_rp_max;       // max over all planes of hist_len
+  int32_t acc_bad;          // some plane's hist_len is outside [0, hist_cap]
+  int32_t pad[50];
 };
 static_assert(sizeof(Ctrl) == 256, "ctrl block is one 256-byte line");
 
 struct Layout {           // byte offsets inside the workspace
-  size_t tile_state, ell, mask, idx, dyn_list, rp_list, rp_len, trig_g, rot_g, trig_h, rot_h, total;
+  size_t tile_state, ell, mask, idx, trig_g, rot_g, trig_h, rot_h, total;
   int32_t max_tiles;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 inline Layout make_layout(int64_t n_tok, int64_t n_planes, int64_t F, int64_t n_t, int64_t max_frames) {
+  (void)n_planes;
   Layout L{};
   size_t off = sizeof(Ctrl);
   L.max_tiles = (int32_t)((n_tok + kMinTile - 1) / kMinTile);
@@ -48,9 +56,6 @@ inline Layout make_layout(int64_t n_tok, int64_t n_planes, int64_t F, int64_t n_
   L.ell = off;        off = align256(off + 4 * (size_t)n_tok);
   L.mask = off;       off = align256(off + (size_t)n_tok);
   L.idx = off;        off = align256(off + 4 * (size_t)n_tok);
-  L.dyn_list = off;   off = align256(off + 4 * (size_t)n_planes);
-  L.rp_list = off;    off = align256(off + 4 * (size_t)n_planes);
-  L.rp_len = off;     off = align256(off + 4 * (size_t)n_planes);
   L.trig_g = off;     off = align256(off + 16 * (size_t)(F * n_t));
   L.rot_g = off;      off = align256(off + (size_t)F);
   L.trig_h = off;     off = align256(off + 16 * (size_t)(max_frames * n_t));
@@ -59,7 +64,7 @@ inline Layout make_layout(int64_t n_tok, int64_t n_planes, int64_t F, int64_t n_
   return L;
 }
 
-// ------------------------------------------------------------------------------------------ scan kernel params
+// ------------------------------------------------------------------------------------------ kernel params
 struct ScanParams {
   // score inputs (x0hat == nullptr -> the mask comes from mask_in)
   const float* x0hat;
@@ -78,23 +83,19 @@ struct ScanParams {
   int32_t* status;
   int32_t* kept_dev;
   int32_t force_timeout;
-  // cache bookkeeping, done by the final CTA
-  int32_t update_cache;   // append kept rows' frames, grow hist_len of dynamic planes
-  int32_t want_rephase;   // list planes whose history must be re-indexed
-  int32_t* hist_len;
-  int32_t* hist_t;
+  // plane checks (CTAs numbered below n_plane_slices each check 256 planes)
+  int32_t update_cache;   // a gather follows: check the receiving planes and the history capacity
+  int32_t want_rephase;   // a re-index follows: find the longest history
+  const int32_t* hist_len;
   const uint8_t* head_is_static;
-  int32_t n_planes;
+  int32_t n_planes, n_plane_slices;
   int64_t hist_cap;
-  int32_t evict_first_frame, T;
-  int32_t* dyn_list;
-  int32_t* rp_list;
-  int32_t* rp_len;
-  // phase tables, built by the CTAs numbered past the tiles
+  // phase tables, built by the CTAs numbered past the tiles (kTableEntries entries each)
   int32_t n_trig_blocks;
   float4* trig_g;          // [F][n_t]: turn from t to t~(t; q0) for the leaving chunk's frames
   uint8_t* rot_g;          // [F]: nonzero if that frame turns at all
   int32_t g_frames;        // F, or 0 when no gather follows
+  int32_t evict_first_frame;
   float4* trig_h;          // [max_frames][n_t]: turn from t~(t; q0_prev) to t~(t; q0)
   uint8_t* rot_h;          // [max_frames]
   int32_t h_lo, h_hi;      // frames [h_lo, h_hi) of the history table (empty when no re-index follows)
@@ -105,22 +106,27 @@ struct ScanParams {
   int32_t q0, q0_prev;
 };
 
+constexpr int kTableEntries = 64;  // table entries per table CTA (fp64 work spread over many SMs)
+constexpr int kSlots = 4;          // 16-byte vectors a thread owns per tensor and plane in the streaming kernels
+
 struct GatherParams {
   char* k;
   char* v;
   int64_t plane_bytes;     // cap * row_bytes
-  int32_t row_bytes;       // D * element size (multiple of 16)
+  int32_t row_bytes;       // D * element size (multiple of 16, at most 16 KiB)
   int32_t vpr;             // 16-byte vectors per row
-  int32_t vpr_shift;       // log2(vpr) when vpr is a power of two, else -1
   int64_t src_row0;        // first row of the leaving chunk's slot
   int64_t dst_row0;        // first history row (sink_rows)
+  int32_t n_planes;
   const Ctrl* ctrl;
   const int32_t* idx;
-  const int32_t* dyn_list;
+  const uint8_t* head_is_static;
+  int32_t* hist_len;       // receiving planes: set to common_len + k
+  int32_t* hist_t;         // positions [common_len, common_len + k) get the kept tokens' frames
+  int32_t evict_first_frame;
   const float4* trig_g;
   const uint8_t* rot_g;
   int32_t T, n_t, dtype;
-  int32_t rows_per_item;
 };
 
 struct RephaseParams {
@@ -129,9 +135,9 @@ struct RephaseParams {
   int32_t row_bytes;
   int32_t nvt;             // 16-byte vectors of a row that hold temporal pairs
   int64_t hist_row0;       // sink_rows
+  int32_t n_planes;
   const Ctrl* ctrl;
-  const int32_t* rp_list;
-  const int32_t* rp_len;
+  const int32_t* hist_len; // read before the gather of the same step grows it
   const int32_t* hist_t;
   const float4* trig_h;
   const uint8_t* rot_h;
@@ -141,8 +147,8 @@ struct RephaseParams {
 };
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s);
-cudaError_t launch_gather(const GatherParams& p, cudaStream_t s);
-cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s);
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch);
+cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch);
 int sm_count();
 
 // ------------------------------------------------------------------------------------------ device helpers
@@ -223,6 +229,25 @@ __device__ __forceinline__ uint4 dev_rotate_vec(uint4 x, int dtype, int p0, int 
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may start while its
+// predecessor drains; it must wait here before it reads anything the predecessor wrote.  Without that launch
+// attribute the wait returns at once.
+__device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
 
 #endif  // __CUDACC__

@@ -6,55 +6,109 @@
 // and only the key phase changes.  Since g depends on q0, the phase of every compressed history key moves whenever
 // q0 advances.
 //
-// Only the 16-byte vectors of a row that hold temporal pairs are read and written (for bf16, D = 128 and
-// n_t = 22 that is the first 96 bytes of each 256-byte row); values and the other key dims are never touched.
-// One thread per (plane, row, vector); rows of frames whose phase does not change are skipped.
+// Only the 16-byte vectors of a row that hold temporal pairs are read and written (for bf16, D = 128 and n_t = 22
+// that is the first 96 bytes of each 256-byte row); values and the other key dims are never touched.  Plane
+// streaming as in the gather: an item is (block of history rows, range of planes); each thread owns kSlots fixed
+// (row, vector) pairs, looks up their frame's table row once, and walks the planes of its range.  Rows whose frame
+// does not move, and rows past a plane's own history length, are skipped.  The kernel runs before the gather of the
+// same step, so hist_len still holds the lengths before the step.
 #include "dcp_internal.cuh"
 
 namespace dcp {
 
 namespace {
 
-__global__ void __launch_bounds__(kThreads) rephase_kernel(const RephaseParams p) {
+__global__ void __launch_bounds__(kThreads, 3) rephase_kernel(const RephaseParams p) {
+  wait_for_predecessor();
+  allow_dependents();
   const Ctrl* c = p.ctrl;
   if (c->abort) return;
-  const int n_rp = c->n_rp, rp_max = c->rp_max;
-  if (n_rp <= 0 || rp_max <= 0) return;
+  const int rp_max = c->rp_max;
+  if (rp_max <= 0 || p.nvt <= 0) return;
   const int ppv = p.dtype == DCP_BF16 ? 4 : 2;
-  const int64_t per_plane = (int64_t)rp_max * p.nvt;
-  const int64_t total = (int64_t)n_rp * per_plane;
-  for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < total; g += (int64_t)gridDim.x * kThreads) {
-    const int i = (int)(g / per_plane);
-    const int64_t rem = g - (int64_t)i * per_plane;
-    const int row = (int)(rem / p.nvt);
-    const int vec = (int)(rem - (int64_t)row * p.nvt);
-    if (row >= __ldg(p.rp_len + i)) continue;
-    const int t = __ldg(p.hist_t + row);
-    if (t < p.h_lo || t >= p.h_hi) {
-      set_status(p.status, DCP_EDEVICE);  // a history frame outside the table: corrupt hist_t, leave the row
-      continue;
+  const int rows_per_item = (kThreads * kSlots) / p.nvt;
+  const int nblk = (rp_max + rows_per_item - 1) / rows_per_item;
+  int ranges = (int)gridDim.x / nblk;
+  if (ranges < 1) ranges = 1;
+  if (ranges > p.n_planes) ranges = p.n_planes;
+  const int ppr = (p.n_planes + ranges - 1) / ranges;
+  const int items = nblk * ranges;
+
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int jb = it % nblk, r = it / nblk;
+    const int p0 = r * ppr, p1 = min(p.n_planes, p0 + ppr);
+    const int j0 = jb * rows_per_item;
+
+    int64_t off[kSlots];
+    int row_of[kSlots], vec_of[kSlots];
+    const float4* trig[kSlots];
+    bool live[kSlots];
+    bool any = false;
+#pragma unroll
+    for (int u = 0; u < kSlots; ++u) {
+      const int e = threadIdx.x + u * kThreads;
+      const int row = e / p.nvt, vec = e - row * p.nvt;
+      row_of[u] = j0 + row;
+      vec_of[u] = vec;
+      live[u] = false;
+      off[u] = 0;
+      trig[u] = p.trig_h;
+      if (row < rows_per_item && j0 + row < rp_max) {
+        const int t = __ldg(p.hist_t + j0 + row);
+        if (t < p.h_lo || t >= p.h_hi) {
+          set_status(p.status, DCP_EDEVICE);  // a history frame outside the table: corrupt hist_t, leave the row
+        } else if (__ldg(p.rot_h + t)) {
+          live[u] = true;
+          trig[u] = p.trig_h + (int64_t)t * p.n_t;
+          off[u] = (p.hist_row0 + j0 + row) * (int64_t)p.row_bytes + vec * 16;
+        }
+      }
+      any |= live[u];
     }
-    if (!__ldg(p.rot_h + t)) continue;
-    const int plane = __ldg(p.rp_list + i);
-    uint4* addr = reinterpret_cast<uint4*>(p.k + (int64_t)plane * p.plane_bytes + (p.hist_row0 + row) * p.row_bytes +
-                                           vec * 16);
-    uint4 x = *addr;
-    x = dev_rotate_vec(x, p.dtype, vec * ppv, p.n_t, p.trig_h + (int64_t)t * p.n_t);
-    *addr = x;
+    if (!__syncthreads_or(any)) continue;
+
+    for (int pl = p0; pl < p1; ++pl) {
+      const int len = __ldg(p.hist_len + pl);
+      if (len <= j0) continue;
+      char* kb = p.k + pl * p.plane_bytes;
+      uint4 x[kSlots];
+      bool go[kSlots];
+#pragma unroll
+      for (int u = 0; u < kSlots; ++u) {
+        go[u] = live[u] && row_of[u] < len;
+        if (go[u]) x[u] = *reinterpret_cast<const uint4*>(kb + off[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kSlots; ++u) {
+        if (go[u]) {
+          x[u] = dev_rotate_vec(x[u], p.dtype, vec_of[u] * ppv, p.n_t, trig[u]);
+          *reinterpret_cast<uint4*>(kb + off[u]) = x[u];
+        }
+      }
+    }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s) {
+cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch) {
   static int blocks_per_sm = 0;
   if (!blocks_per_sm) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, rephase_kernel, kThreads, 0) != cudaSuccess ||
         blocks_per_sm < 1)
       blocks_per_sm = 1;
   }
-  rephase_kernel<<<sm_count() * blocks_per_sm, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sm_count() * blocks_per_sm));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_launch ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, rephase_kernel, p);
 }
 
 }  // namespace dcp

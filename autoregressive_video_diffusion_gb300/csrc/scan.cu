@@ -12,8 +12,13 @@
 //               DCP_ETIMEOUT and the whole call is abandoned), then write their kept positions.
 //   table CTAs  build the cos/sin tables of the key re-phase (section "what differs": t~(t) = q0 - g(q0 - t)) in
 //               double precision, stored as float hi/lo pairs.
-//   final CTA   (the last to finish) reads the kept count, lists the planes to gather and to re-index, checks the
-//               history capacity, grows hist_len / hist_t, and resets the scan state for the next call.
+//   plane checks the CTAs numbered below ceil(planes / 256) also read 256 planes' hist_len each and fold them into
+//               warp-reduced atomic maxima (receiving planes' shortest and longest history, lowest receiving plane,
+//               longest history of any plane).
+//   final CTA   (the last to finish) reads the kept count and the plane checks, decides capacity and consistency,
+//               publishes the verdict for the kernels that follow, and resets the scan state for the next call.
+// The kernel lets its dependents launch early (programmatic dependent launch); they wait for it to finish before
+// they read anything it wrote.
 #include "dcp_internal.cuh"
 
 namespace dcp {
@@ -183,8 +188,43 @@ __device__ void tile_work(const ScanParams& p, int tile_id, TileShared& sh) {
   if (keep && p.idx_out && !sh.timed_out) p.idx_out[sh.excl + local] = t0 + tid;
 }
 
+__device__ void plane_checks(const ScanParams& p, int slice) {
+  const int pl = slice * kThreads + threadIdx.x;
+  int len1 = 0, min_inv = 0, first_inv = 0, longest = 0, bad = 0;
+  if (pl < p.n_planes) {
+    const int len = p.hist_len[pl];
+    if (len < 0 || len > p.hist_cap) {
+      bad = 1;
+    } else {
+      longest = len;
+      const bool receives = p.update_cache && !(p.head_is_static && p.head_is_static[pl]);
+      if (receives) {
+        len1 = len + 1;
+        min_inv = INT32_MAX - len;
+        first_inv = INT32_MAX - pl;
+      }
+    }
+  }
+  len1 = __reduce_max_sync(kFull, len1);
+  min_inv = __reduce_max_sync(kFull, min_inv);
+  first_inv = __reduce_max_sync(kFull, first_inv);
+  longest = __reduce_max_sync(kFull, longest);
+  bad = __reduce_max_sync(kFull, bad);
+  if ((threadIdx.x & 31) == 0) {
+    Ctrl* c = p.ctrl;
+    if (len1) {
+      atomicMax(&c->acc_len_max1, len1);
+      atomicMax(&c->acc_len_min_inv, min_inv);
+      atomicMax(&c->acc_first_inv, first_inv);
+    }
+    if (longest) atomicMax(&c->acc_rp_max, longest);
+    if (bad) atomicMax(&c->acc_bad, 1);
+  }
+}
+
 __device__ void table_work(const ScanParams& p, int block) {
-  const int e = block * kThreads + threadIdx.x;
+  if (threadIdx.x >= kTableEntries) return;
+  const int e = block * kTableEntries + threadIdx.x;
   const int n_g = p.g_frames * p.n_t;
   const int n_h = (p.h_hi - p.h_lo) * p.n_t;
   if (e < n_g) {
@@ -207,13 +247,12 @@ __device__ void table_work(const ScanParams& p, int block) {
   }
 }
 
+__device__ __forceinline__ int vload(const int32_t* x) { return *reinterpret_cast<const volatile int32_t*>(x); }
+
 __device__ void finalize(const ScanParams& p) {
   Ctrl* c = p.ctrl;
-  __shared__ int s_warp_a[kThreads / 32], s_warp_b[kThreads / 32];
-  __shared__ int s_abort, s_k, s_ndyn, s_nrp, s_rpmax, s_minlen, s_maxlen;
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    int abort = *reinterpret_cast<volatile int*>(&c->tile_error) ? 1 : 0;
+  if (threadIdx.x == 0) {
+    int abort = vload(&c->tile_error) ? 1 : 0;
     int k = 0;
     if (!abort && p.n_tiles > 0) {
       const unsigned long long st = ld_acquire_u64(p.tile_state + p.n_tiles - 1);
@@ -224,82 +263,54 @@ __device__ void finalize(const ScanParams& p) {
         set_status(p.status, DCP_ETIMEOUT);
       }
     }
-    s_abort = abort;
-    s_k = k;
-    s_ndyn = 0;
-    s_nrp = 0;
-    s_rpmax = 0;
-    s_minlen = 0x7FFFFFFF;
-    s_maxlen = -1;
-  }
-  __syncthreads();
-
-  if ((p.update_cache || p.want_rephase) && !s_abort) {
-    for (int base = 0; base < p.n_planes; base += kThreads) {
-      const int pl = base + tid;
-      const bool valid = pl < p.n_planes;
-      const int len = valid ? __ldcg(p.hist_len + pl) : 0;
-      const bool is_static = valid && p.head_is_static && p.head_is_static[pl];
-      const int dyn = (valid && !is_static && p.update_cache) ? 1 : 0;
-      const int rp = (valid && len > 0 && p.want_rephase) ? 1 : 0;
-      int tot_d = 0, tot_r = 0;
-      const int od = block_exclusive_scan(dyn, s_warp_a, &tot_d);
-      const int orp = block_exclusive_scan(rp, s_warp_b, &tot_r);
-      if (dyn) {
-        p.dyn_list[s_ndyn + od] = pl;
-        atomicMin(&s_minlen, len);
-        atomicMax(&s_maxlen, len);
-      }
-      if (rp) {
-        p.rp_list[s_nrp + orp] = pl;
-        p.rp_len[s_nrp + orp] = len;
-        atomicMax(&s_rpmax, len);
-      }
-      __syncthreads();
-      if (tid == 0) {
-        s_ndyn += tot_d;
-        s_nrp += tot_r;
-      }
-      __syncthreads();
+    const int len1 = vload(&c->acc_len_max1), min_inv = vload(&c->acc_len_min_inv);
+    const int first_inv = vload(&c->acc_first_inv), longest = vload(&c->acc_rp_max), bad = vload(&c->acc_bad);
+    const bool has_dyn = p.update_cache && len1 > 0;
+    int common = 0, first = -1;
+    if ((p.update_cache || p.want_rephase) && bad && !abort) {
+      abort = 1;
+      set_status(p.status, DCP_EDEVICE);
     }
-    if (tid == 0 && p.update_cache && s_ndyn > 0) {
-      if (s_minlen != s_maxlen) {
-        s_abort = 1;
+    if (has_dyn) {
+      const int max_len = len1 - 1, min_len = INT32_MAX - min_inv;
+      common = min_len;
+      first = INT32_MAX - first_inv;
+      if (!abort && min_len != max_len) {
+        abort = 1;
         set_status(p.status, DCP_EDEVICE);
-      } else if ((int64_t)s_minlen + s_k > p.hist_cap) {
-        s_abort = 1;
+      } else if (!abort && (int64_t)min_len + k > p.hist_cap) {
+        abort = 1;
         set_status(p.status, DCP_ECAPACITY);
       }
     }
-  }
-  __syncthreads();
-
-  const int common = s_ndyn > 0 ? s_minlen : 0;
-  if (p.update_cache && !s_abort && s_ndyn > 0) {
-    for (int i = tid; i < s_ndyn; i += kThreads) p.hist_len[p.dyn_list[i]] = common + s_k;
-    for (int j = tid; j < s_k; j += kThreads) p.hist_t[common + j] = p.evict_first_frame + __ldcg(p.idx_out + j) / p.T;
-  }
-  for (int i = tid; i < p.n_tiles; i += kThreads) p.tile_state[i] = 0ull;
-  if (tid == 0) {
-    c->k = s_k;
-    c->n_dyn = p.update_cache ? s_ndyn : 0;
+    c->k = k;
+    c->has_dyn = has_dyn ? 1 : 0;
     c->common_len = common;
-    c->n_rp = s_nrp;
-    c->rp_max = s_rpmax;
-    c->abort = s_abort;
+    c->first_dyn = first;
+    c->rp_max = p.want_rephase ? longest : 0;
+    c->abort = abort;
+    if (p.kept_dev) *p.kept_dev = k;
+    c->acc_len_max1 = 0;
+    c->acc_len_min_inv = 0;
+    c->acc_first_inv = 0;
+    c->acc_rp_max = 0;
+    c->acc_bad = 0;
     c->tile_error = 0;
-    if (p.kept_dev) *p.kept_dev = s_k;
     c->ticket = 0u;
     c->done = 0u;
   }
+  __syncthreads();  // thread 0 has read the last tile's state; only now may the states be cleared
+  for (int i = threadIdx.x; i < p.n_tiles; i += kThreads) p.tile_state[i] = 0ull;
 }
 
 __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanParams p) {
   __shared__ TileShared sh;
   __shared__ int s_id, s_last;
+  allow_dependents();
   if (threadIdx.x == 0) s_id = (int)atomicAdd(&p.ctrl->ticket, 1u);
   __syncthreads();
   const int id = s_id;
+  if (id < p.n_plane_slices) plane_checks(p, id);
   if (id < p.n_tiles) tile_work(p, id, sh);
   else if (id - p.n_tiles < p.n_trig_blocks) table_work(p, id - p.n_tiles);
 
@@ -317,6 +328,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanParams p) {
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
   int grid = p.n_tiles + p.n_trig_blocks;
+  if (grid < p.n_plane_slices) grid = p.n_plane_slices;
   if (grid < 1) grid = 1;
   scan_kernel<<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
