@@ -76,7 +76,6 @@ _SIGS = {
     "dcp_abi_struct_sizes": ([], ctypes.c_uint32),
     "dcp_set_phase_events": ([_vp, _vp], _i32),
     "dcp_prune_step_noalloc": ([_pc, _pg, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
-    "dcp_debug_force_scan_timeout": ([_i32], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -266,7 +265,3 @@ def dcp_set_phase_events(ev_after_scan, ev_after_gather) -> None:
     a = None if ev_after_scan is None else ev_after_scan.cuda_event
     b = None if ev_after_gather is None else ev_after_gather.cuda_event
     _check(lib.dcp_set_phase_events(a, b), "dcp_set_phase_events")
-
-
-def dcp_debug_force_scan_timeout(on: bool) -> bool:
-    return bool(lib.dcp_debug_force_scan_timeout(1 if on else 0))

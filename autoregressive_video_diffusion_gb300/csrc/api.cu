@@ -9,7 +9,6 @@ using namespace dcp;
 
 namespace {
 
-int g_force_timeout = 0;
 cudaEvent_t g_ev_after_scan = nullptr;
 cudaEvent_t g_ev_after_gather = nullptr;
 
@@ -103,9 +102,8 @@ ScanParams cache_scan_params(const dcp_cache* c, const dcp_config* g, const Deri
   sp.gamma = g->gamma;
   sp.keep_rule = g->keep_rule;
   sp.ctrl = at<Ctrl>(ws, 0);
-  sp.tile_state = at<unsigned long long>(ws, d.lay.tile_state);
+  sp.bits = at<uint32_t>(ws, d.lay.bits);
   sp.status = c->status;
-  sp.force_timeout = g_force_timeout;
   sp.hist_len = c->hist_len;
   sp.n_planes = (int32_t)d.n_planes;
   sp.n_plane_slices = (int32_t)((d.n_planes + kThreads - 1) / kThreads);
@@ -234,10 +232,9 @@ dcp_status dcp_score_mask(const float* x0hat, const float* xref, int32_t n_tok, 
   sp.mask_out = mask_dev;
   sp.idx_out = idx_dev;
   sp.ctrl = at<Ctrl>(ws, 0);
-  sp.tile_state = at<unsigned long long>(ws, lay.tile_state);
+  sp.bits = at<uint32_t>(ws, lay.bits);
   sp.status = status_dev;
   sp.kept_dev = kept_dev;
-  sp.force_timeout = g_force_timeout;
   return cuda_ok(launch_scan(sp, (cudaStream_t)stream));
 }
 
@@ -372,7 +369,7 @@ const char* dcp_status_string(dcp_status s) {
     case DCP_EINVAL: return "invalid argument";
     case DCP_ECAPACITY: return "history capacity exceeded";
     case DCP_ECUDA: return "CUDA runtime error";
-    case DCP_ETIMEOUT: return "index scan wait timed out";
+    case DCP_ETIMEOUT: return "timed out (not produced by this version)";
     case DCP_EDEVICE: return "inconsistent cache state on the device";
     default: return "unknown status";
   }
@@ -398,10 +395,5 @@ dcp_status dcp_set_phase_events(void* ev_after_scan, void* ev_after_gather) {
 
 uint32_t dcp_abi_struct_sizes(void) { return ((uint32_t)sizeof(dcp_cache) << 16) | (uint32_t)sizeof(dcp_config); }
 
-int32_t dcp_debug_force_scan_timeout(int32_t on) {
-  int32_t prev = g_force_timeout;
-  g_force_timeout = on ? 1 : 0;
-  return prev;
-}
 
 }  // extern "C"

@@ -10,20 +10,15 @@
 namespace dcp {
 
 constexpr int kThreads = 256;          // every kernel of the library runs 256-thread CTAs
-constexpr int kMaxTile = 256;          // tokens per scan tile (one token per thread in the scan phase)
-constexpr int kMinTile = 32;
-constexpr uint32_t kFlagAgg = 1u;      // tile published its own count
-constexpr uint32_t kFlagPrefix = 2u;   // tile published its inclusive prefix
-constexpr int kSpinLimit = 1 << 22;    // bounded look-back wait (x ~64 ns backoff -> well under a second)
-constexpr int kForcedSpinLimit = 4096;
+constexpr int kMaxTile = 256;          // tokens per scan tile (one token per thread in the mask phase)
 
 // Control block at the start of the workspace.  The scan kernel's final CTA writes the verdict fields, which the
-// re-index and gather kernels that follow it on the stream read.  Counters and accumulators start at zero (a zeroed
-// workspace) and the final CTA puts them back to zero at the end of every call.
+// re-index and gather kernels that follow it on the stream read.  The completion counter and the accumulators start
+// at zero (a zeroed workspace) and the final CTA puts them back to zero at the end of every call.
 struct Ctrl {
-  uint32_t ticket;          // dynamic CTA numbering of the scan kernel
   uint32_t done;            // CTAs of the scan kernel that finished
-  int32_t tile_error;       // a tile's bounded wait gave up during this call
+  int32_t reserved0;
+  int32_t reserved1;
   int32_t abort;            // verdict: nonzero -> the later kernels of the call do nothing
   int32_t k;                // kept tokens
   int32_t has_dyn;          // at least one plane receives the kept rows
@@ -41,8 +36,7 @@ struct Ctrl {
 static_assert(sizeof(Ctrl) == 256, "ctrl block is one 256-byte line");
 
 struct Layout {           // byte offsets inside the workspace
-  size_t tile_state, ell, mask, idx, trig_g, rot_g, trig_h, rot_h, total;
-  int32_t max_tiles;
+  size_t bits, ell, mask, idx, trig_g, rot_g, trig_h, rot_h, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -51,8 +45,7 @@ inline Layout make_layout(int64_t n_tok, int64_t n_planes, int64_t F, int64_t n_
   (void)n_planes;
   Layout L{};
   size_t off = sizeof(Ctrl);
-  L.max_tiles = (int32_t)((n_tok + kMinTile - 1) / kMinTile);
-  L.tile_state = off; off = align256(off + sizeof(unsigned long long) * (size_t)L.max_tiles);
+  L.bits = off;       off = align256(off + 4 * (size_t)((n_tok + 31) / 32));
   L.ell = off;        off = align256(off + 4 * (size_t)n_tok);
   L.mask = off;       off = align256(off + (size_t)n_tok);
   L.idx = off;        off = align256(off + 4 * (size_t)n_tok);
@@ -79,10 +72,9 @@ struct ScanParams {
   int32_t* idx_out;
   // control
   Ctrl* ctrl;
-  unsigned long long* tile_state;
+  uint32_t* bits;          // keep mask as ballot words, one bit per token
   int32_t* status;
   int32_t* kept_dev;
-  int32_t force_timeout;
   // plane checks (CTAs numbered below n_plane_slices each check 256 planes)
   int32_t update_cache;   // a gather follows: check the receiving planes and the history capacity
   int32_t want_rephase;   // a re-index follows: find the longest history

@@ -18,10 +18,11 @@
  *     named *_host are host pointers.  The library never allocates, frees or keeps any pointer past the call.
  *   - `stream` is a cudaStream_t passed as void*.  Every call is asynchronous on that stream.
  *   - Host-detectable errors (null or misaligned pointers, bad sizes, bad config) return before any launch and
- *     change nothing.  Errors only the device can see (history capacity exceeded, inconsistent head lengths, a
- *     bounded wait that gave up) are written to the cache's (or the caller's) device status word; nothing traps.
- *     Read it with dcp_get_status().  A step that sets a device error leaves the cache contents and lengths as
- *     they were.
+ *     change nothing.  Errors only the device can see (history capacity exceeded, inconsistent head lengths or
+ *     history frames) are written to the cache's device status word; nothing traps.
+ *     Read it with dcp_get_status().  A step refused for capacity or inconsistent lengths leaves the cache contents
+ *     and lengths as they were; a history frame outside [first non-sink frame, q0) is found while re-indexing, and
+ *     only that row is left unturned.
  *   - The workspace is caller-owned device scratch of dcp_workspace_size() bytes, 256-byte aligned.  Zero it once
  *     with dcp_workspace_init() before its first use; every call leaves it ready for the next.  Calls that share a
  *     workspace or a cache must be ordered on one stream (not thread-safe per workspace or cache).
@@ -52,7 +53,7 @@ typedef int32_t dcp_status;
 #define DCP_EINVAL 1    /* invalid argument, detected on the host before any launch */
 #define DCP_ECAPACITY 2 /* device: history would exceed hist_cap; the step was skipped */
 #define DCP_ECUDA 3     /* a CUDA runtime call failed */
-#define DCP_ETIMEOUT 4  /* device: a bounded wait of the index scan gave up; outputs of that call are invalid */
+#define DCP_ETIMEOUT 4  /* reserved: the kernels of this version contain no waits, so nothing times out */
 #define DCP_EDEVICE 5   /* device: dynamic heads disagree on hist_len (corrupt cache state); the step was skipped */
 
 #define DCP_BF16 0
@@ -105,7 +106,7 @@ dcp_status dcp_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream
  *   mask_dev  (nullable): uint8 [n_tok] out, 1 = keep (rule from keep_rule).
  *   idx_dev   (nullable): int32 [n_tok] out, increasing kept positions in [0, kept).
  *   kept_dev  (nullable): int32 out, number of kept tokens.
- *   status_dev          : int32 device status word (DCP_ETIMEOUT if a bounded wait gave up).
+ *   status_dev          : int32 device status word (no device error is produced by this call today).
  * Errors: DCP_EINVAL for null inputs, n_tok < 1 or > 2^30, d < 1, non-finite gamma, short workspace. */
 dcp_status dcp_score_mask(const float* x0hat_dev, const float* xref_dev, int32_t n_tok, int32_t d, float gamma,
                           int32_t keep_rule, float* ell_dev, uint8_t* mask_dev, int32_t* idx_dev, int32_t* kept_dev,
@@ -197,9 +198,6 @@ dcp_status dcp_set_phase_events(void* ev_after_scan, void* ev_after_gather);
 /* ABI check for bindings: (sizeof(dcp_cache) << 16) | sizeof(dcp_config). */
 uint32_t dcp_abi_struct_sizes(void);
 
-/* Test hook: when on != 0, index-scan tiles stop publishing their counts, so every later tile's bounded wait runs
- * out and the call reports DCP_ETIMEOUT (no hang, no trap).  Returns the previous setting. */
-int32_t dcp_debug_force_scan_timeout(int32_t on);
 
 #ifdef __cplusplus
 }

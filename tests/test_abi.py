@@ -131,11 +131,6 @@ def test_invalid_other_entry_points_rejected():
     assert L.dcp_reset_status(None, None) == 1
 
 
-def test_debug_hook_round_trip():
-    prev = dcp.dcp_debug_force_scan_timeout(True)
-    assert dcp.dcp_debug_force_scan_timeout(prev) is True
-
-
 def test_seeded_inputs_clear_of_tie_band():
     """Every seeded score input of the workloads keeps |l - gamma| >= 1e-6, so the kernel's fp32 sum and the
     oracle's double sum take the same keep decision and masks can be compared exactly."""

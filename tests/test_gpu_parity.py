@@ -222,41 +222,58 @@ def test_inconsistent_lengths_detected(gpu):
     assert np.array_equal(before.k, after.k) and np.array_equal(before.hist_len, after.hist_len)
 
 
-def test_forced_scan_timeout_reports_and_recovers(gpu):
-    """The look-back wait is bounded: with publication switched off every later tile gives up, the call reports
-    DCP_ETIMEOUT, leaves the cache alone, and the next call on the same workspace works."""
-    w = scaled(TINY_ROT, tokens_per_frame=640, hist_cap=5 * 640)   # 640 tokens: three scan tiles of 256
+def test_corrupt_history_detected(gpu):
+    """A history length outside [0, hist_cap] or a history frame outside the phase table is reported as
+    DCP_EDEVICE and nothing moves (no trap)."""
+    w = TINY_ROT
     hc, (c, q0_prev, q0) = replay.state_before_last(w)
-    n_tok, d = 6240, 64
-    x = synth.normal_f32(n_tok * d, 5, 1).reshape(n_tok, d)
-    x0 = (x + np.float32(0.5) * synth.normal_f32(n_tok * d, 5, 2).reshape(n_tok, d)).astype(np.float32)
-    ws = dcp.new_workspace(dcp.dcp_score_workspace_size(n_tok))
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kept = torch.zeros(1, dtype=torch.int32, device="cuda")
-    idx = torch.zeros(n_tok, dtype=torch.int32, device="cuda")
-    prev = dcp.dcp_debug_force_scan_timeout(True)
-    try:
-        dcp.dcp_score_mask(_cuda(x0), _cuda(x), 0.1, 0, None, None, idx, kept, status, ws)
-        assert dcp.dcp_get_status(status) == dcp.DCP_ETIMEOUT
-        # a cache step under the same switch: refused, cache untouched
-        dev = devcache.to_device(hc, w)
+    x0, xr = w.score_inputs(c)
+    for corrupt in ("len", "frame"):
+        bad = hc.copy()
+        if corrupt == "len":
+            bad.hist_len[:] = w.hist_cap + 1
+        else:
+            bad.hist_t[0] = q0 + 5   # a frame that is not even in the past
+        dev = devcache.to_device(bad, w)
         gcfg = devcache.dcp_config(w)
-        wsc = dcp.new_workspace(dcp.dcp_workspace_size(dev, gcfg))
+        ws = dcp.new_workspace(dcp.dcp_workspace_size(dev, gcfg))
         before = devcache.from_device(dev, w)
-        x0c, xrc = w.score_inputs(c)
-        dcp.dcp_prune_step(dev, gcfg, _cuda(x0c), _cuda(xrc), w.slot_of(c), w.first_frame(c), q0_prev, q0, None, None,
-                           None, wsc)
-        assert dcp.dcp_get_status(dev.status) == dcp.DCP_ETIMEOUT
+        dcp.dcp_prune_step(dev, gcfg, _cuda(x0), _cuda(xr), w.slot_of(c), w.first_frame(c), q0_prev, q0, None, None,
+                           None, ws)
+        assert dcp.dcp_get_status(dev.status) == dcp.DCP_EDEVICE, corrupt
         after = devcache.from_device(dev, w)
-        assert np.array_equal(before.k, after.k) and np.array_equal(before.v, after.v)
-        assert np.array_equal(before.hist_len, after.hist_len)
-    finally:
-        dcp.dcp_debug_force_scan_timeout(prev)
-    dcp.dcp_reset_status(status)
-    dcp.dcp_score_mask(_cuda(x0), _cuda(x), 0.1, 0, None, None, idx, kept, status, ws)
-    assert dcp.dcp_get_status(status) == dcp.DCP_OK
-    ref = oracle.indices(oracle.keep(oracle.score(x0, x)))
-    assert int(kept.item()) == len(ref) and np.array_equal(idx[: len(ref)].cpu().numpy(), ref)
+        if corrupt == "len":
+            assert np.array_equal(before.k, after.k) and np.array_equal(before.hist_len, after.hist_len)
+        else:
+            # only the row whose frame is outside the table is left alone by the re-index; the rest proceeds
+            assert np.array_equal(before.k[:, :, w.sink_rows], after.k[:, :, w.sink_rows])
+
+
+def test_one_workspace_serves_every_entry_point(gpu):
+    """The workspace comes back ready after every call: score-only, re-index, compaction and full steps interleaved
+    on one workspace give the oracle's results."""
+    w = TINY_ROT
+    hc, (c, q0_prev, q0) = replay.state_before_last(w)
+    dev = devcache.to_device(hc, w)
+    gcfg = devcache.dcp_config(w)
+    ws = dcp.new_workspace(dcp.dcp_workspace_size(dev, gcfg))
+    x0, xr = w.score_inputs(c)
+    n = w.C
+    kept = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = torch.zeros(n, dtype=torch.int32, device="cuda")
+    ref_idx = oracle.indices(oracle.keep(oracle.score(x0, xr)))
+    for _ in range(3):
+        dcp.dcp_score_mask(_cuda(x0), _cuda(xr), w.gamma, 0, None, None, idx, kept, dev.status, ws)
+        assert int(kept.item()) == len(ref_idx) and np.array_equal(idx[: len(ref_idx)].cpu().numpy(), ref_idx)
+    o = hc.copy()
+    dcp.dcp_rope_reindex(dev, gcfg, q0_prev, q0, ws)
+    assert oracle.rope_reindex(o, replay.cfg_of(w), q0_prev, q0) == oracle.OK
+    dcp.dcp_score_mask(_cuda(x0), _cuda(xr), w.gamma, 0, None, None, idx, kept, dev.status, ws)
+    mask = oracle.keep(oracle.score(x0, xr))
+    dcp.dcp_compact_layers(dev, gcfg, w.slot_of(c), w.first_frame(c), _cuda(mask), None, q0, kept, ws)
+    rc, _ = oracle.compact_layers(o, replay.cfg_of(w), w.slot_of(c), w.first_frame(c), mask, None, q0)
+    assert rc == oracle.OK and dcp.dcp_get_status(dev.status) == dcp.DCP_OK
+    assert_cache_parity(devcache.from_device(dev, w), o, w)
 
 
 # ------------------------------------------------------------------------------------------ full-size single eviction
