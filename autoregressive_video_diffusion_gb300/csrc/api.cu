@@ -27,7 +27,8 @@ dcp_status check_cache_cfg(const dcp_cache* c, const dcp_config* g, Derived* d) 
   if (c->L < 1 || c->H < 1 || c->D < 2 || (c->D & 1)) return DCP_EINVAL;
   if (c->dtype != DCP_BF16 && c->dtype != DCP_F32) return DCP_EINVAL;
   const int es = c->dtype == DCP_BF16 ? 2 : 4;
-  if (((int64_t)c->D * es) % 16 || (int64_t)c->D * es > 16384) return DCP_EINVAL;
+  // rows of at most 4 KiB (a CTA of the streaming kernels covers whole rows), a multiple of 16 bytes
+  if (((int64_t)c->D * es) % 16 || (int64_t)c->D * es > 4096) return DCP_EINVAL;
   if (!aligned(c->k, 16) || !aligned(c->v, 16) || !aligned(c->hist_len, 4) || !aligned(c->hist_t, 4) ||
       !aligned(c->status, 4))
     return DCP_EINVAL;
@@ -52,6 +53,8 @@ dcp_status check_cache_cfg(const dcp_cache* c, const dcp_config* g, Derived* d) 
   if (c->cap < need) return DCP_EINVAL;
   const int64_t T_s = (int64_t)g->sink_chunks * g->frames_per_chunk;
   if (T_s > INT32_MAX) return DCP_EINVAL;
+  // offsets inside one chunk's rows and inside the history region are 32-bit in the kernels
+  if (C * c->D * es >= (int64_t(1) << 31) || c->hist_cap * c->D * es >= (int64_t(1) << 31)) return DCP_EINVAL;
   if (d) {
     d->C = C;
     d->sink_rows = sink_rows;
@@ -126,6 +129,11 @@ void finish_tables(ScanParams& sp) {
   sp.n_trig_blocks = (entries + kTableEntries - 1) / kTableEntries;
 }
 
+// 32-byte vector accesses need 32-byte aligned rows and bases; otherwise the kernels use 16-byte vectors.
+int vector_bytes(const dcp_cache* c, int row_bytes) {
+  return (row_bytes % 32 == 0 && aligned(c->k, 32) && aligned(c->v, 32)) ? 32 : 16;
+}
+
 GatherParams gather_params(const dcp_cache* c, const dcp_config* g, const Derived& d, void* ws, int32_t slot,
                            const uint8_t* head_is_static, int32_t evict_first_frame) {
   GatherParams gp{};
@@ -133,7 +141,7 @@ GatherParams gather_params(const dcp_cache* c, const dcp_config* g, const Derive
   gp.v = static_cast<char*>(c->v);
   gp.row_bytes = c->D * d.esize;
   gp.plane_bytes = c->cap * (int64_t)gp.row_bytes;
-  gp.vpr = gp.row_bytes / 16;
+  gp.vb = vector_bytes(c, gp.row_bytes);
   gp.src_row0 = d.win_row0 + (int64_t)slot * d.C;
   gp.dst_row0 = d.sink_rows;
   gp.n_planes = (int32_t)d.n_planes;
@@ -157,7 +165,8 @@ RephaseParams rephase_params(const dcp_cache* c, const dcp_config* g, const Deri
   rp.k = static_cast<char*>(c->k);
   rp.row_bytes = c->D * d.esize;
   rp.plane_bytes = c->cap * (int64_t)rp.row_bytes;
-  rp.nvt = (2 * g->n_temporal_pairs * d.esize + 15) / 16;
+  rp.vb = vector_bytes(c, rp.row_bytes);
+  rp.nvt = (2 * g->n_temporal_pairs * d.esize + rp.vb - 1) / rp.vb;
   rp.hist_row0 = d.sink_rows;
   rp.n_planes = (int32_t)d.n_planes;
   rp.ctrl = at<Ctrl>(ws, 0);

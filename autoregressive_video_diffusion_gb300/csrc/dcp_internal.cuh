@@ -99,14 +99,16 @@ struct ScanParams {
 };
 
 constexpr int kTableEntries = 64;  // table entries per table CTA (fp64 work spread over many SMs)
-constexpr int kSlots = 4;          // 16-byte vectors a thread owns per tensor and plane in the streaming kernels
+// The streaming kernels move 64 bytes per thread, tensor and plane: four 16-byte vectors, or two 32-byte vectors
+// when rows and base addresses are 32-byte aligned.
+constexpr int kBytesPerThread = 64;
 
 struct GatherParams {
   char* k;
   char* v;
   int64_t plane_bytes;     // cap * row_bytes
   int32_t row_bytes;       // D * element size (multiple of 16, at most 16 KiB)
-  int32_t vpr;             // 16-byte vectors per row
+  int32_t vb;              // bytes per vector: 32 when rows and bases are 32-byte aligned, else 16
   int64_t src_row0;        // first row of the leaving chunk's slot
   int64_t dst_row0;        // first history row (sink_rows)
   int32_t n_planes;
@@ -125,7 +127,8 @@ struct RephaseParams {
   char* k;
   int64_t plane_bytes;
   int32_t row_bytes;
-  int32_t nvt;             // 16-byte vectors of a row that hold temporal pairs
+  int32_t vb;              // bytes per vector (16 or 32)
+  int32_t nvt;             // vectors of a row that hold temporal pairs
   int64_t hist_row0;       // sink_rows
   int32_t n_planes;
   const Ctrl* ctrl;
@@ -193,29 +196,37 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Rotate the pairs held in one 16-byte vector.  p0 = index of its first pair; pairs >= n_t are left as stored.
-// trig points at the table row of the key's frame.
-__device__ __forceinline__ uint4 dev_rotate_vec(uint4 x, int dtype, int p0, int n_t, const float4* trig) {
+// A vector of NW 32-bit words (NW = 4: 16 bytes, NW = 8: 32 bytes) moved by one load or store instruction.
+template <int NW>
+struct Vec {
+  uint32_t w[NW];
+};
+
+// Rotate the pairs held in one vector.  p0 = index of its first pair; pairs >= n_t are left as stored.  trig points
+// at the table row of the key's frame.  bf16: word i holds pair p0 + i; fp32: words 2i, 2i+1 hold pair p0 + i.
+template <int NW>
+__device__ __forceinline__ void dev_rotate_vec(Vec<NW>& x, int dtype, int p0, int n_t, const float4* trig) {
   if (dtype == DCP_BF16) {
-    uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      int p = p0 + i;
+    for (int i = 0; i < NW; ++i) {
+      const int p = p0 + i;
       if (p < n_t) {
         float oa, ob;
-        dev_rotate(bf16lo(w[i]), bf16hi(w[i]), trig[p], oa, ob);
-        w[i] = pack_bf16x2(oa, ob);
+        dev_rotate(bf16lo(x.w[i]), bf16hi(x.w[i]), trig[p], oa, ob);
+        x.w[i] = pack_bf16x2(oa, ob);
       }
     }
-    return make_uint4(w[0], w[1], w[2], w[3]);
   } else {
-    float f[4] = {__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)};
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      int p = p0 + i;
-      if (p < n_t) dev_rotate(f[2 * i], f[2 * i + 1], trig[p], f[2 * i], f[2 * i + 1]);
+    for (int i = 0; i < NW / 2; ++i) {
+      const int p = p0 + i;
+      if (p < n_t) {
+        float oa, ob;
+        dev_rotate(__uint_as_float(x.w[2 * i]), __uint_as_float(x.w[2 * i + 1]), trig[p], oa, ob);
+        x.w[2 * i] = __float_as_uint(oa);
+        x.w[2 * i + 1] = __float_as_uint(ob);
+      }
     }
-    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
   }
 }
 
@@ -229,17 +240,42 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
 __device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
+// Streaming copies: data read once (no L1 allocation) and written once.  The 32-byte forms (sm_100 and later) also
+// mark the lines evict-first in L2.
+__device__ __forceinline__ void ld_stream(Vec<4>& v, const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
                : "l"(p));
-  return v;
 }
 
-__device__ __forceinline__ void st_stream(void* p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+__device__ __forceinline__ void ld_stream(Vec<8>& v, const void* p) {
+  asm volatile("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+                 "=r"(v.w[6]), "=r"(v.w[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void st_stream(void* p, const Vec<4>& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
+               "r"(v.w[3])
                : "memory");
+}
+
+__device__ __forceinline__ void st_stream(void* p, const Vec<8>& v) {
+  asm volatile("st.global.L1::no_allocate.L2::evict_first.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
+               "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+               : "memory");
+}
+
+// In-place (read-modify-write) accesses of the re-index kernel: plain cached loads and stores.
+template <int NW>
+__device__ __forceinline__ void ld_plain(Vec<NW>& v, const void* p) {
+  v = *reinterpret_cast<const Vec<NW>*>(p);
+}
+
+template <int NW>
+__device__ __forceinline__ void st_plain(void* p, const Vec<NW>& v) {
+  *reinterpret_cast<Vec<NW>*>(p) = v;
 }
 
 #endif  // __CUDACC__

@@ -9,11 +9,15 @@
 //
 // Work decomposition ("plane streaming"): the mask is shared by every plane, so the kept rows of one block of the
 // index list sit at the same offsets in every plane.  An item is (block of rows, range of planes).  Each thread owns
-// kSlots fixed 16-byte vectors of the block (row, vector-in-row), computes their source and destination offsets once
-// from the index list, then walks the planes of its range issuing 2 * kSlots independent 16-byte loads (K and V) per
-// plane with no dependent load in between.  Stores of a block are contiguous (the history tail).  Every source
-// vector is read once and every destination vector written once.  Key vectors that hold temporal pairs are turned
-// with the frame's cos/sin table before they are stored.
+// a few fixed vectors of the block (32-byte vectors when rows and bases allow it, else 16-byte), computes their source
+// and destination offsets once from the index list, then walks the planes of its range issuing independent loads of
+// K and V per plane with no dependent load in between; a block's destination rows are one contiguous run.  Every
+// source vector is read once and every destination vector written once.
+//
+// Slot mapping: the threads of one slot cover whole rows (vpr consecutive threads per row); slot u of lane l takes
+// vector (l + u * vpr / slots) mod vpr of its row, so the vectors that hold temporal pairs (the first few of a row)
+// are spread over the threads instead of landing on the same lanes in every slot.  Key vectors with temporal pairs
+// are turned with the frame's cos/sin table before they are stored.
 //
 // Bookkeeping folded in: the item holding the first block of a receiving plane sets its hist_len to
 // common_len + k, and the items of the lowest receiving plane append the kept frames to hist_t.
@@ -23,7 +27,12 @@ namespace dcp {
 
 namespace {
 
-__global__ void __launch_bounds__(kThreads, 4) gather_kernel(const GatherParams p) {
+// 3 CTAs per SM (up to 85 registers): the 4-CTA cap spills the rotation temporaries (measured: equal speed on
+// copies, 5 us slower on a full-depth step whose keys all turn).
+template <int NW>
+__global__ void __launch_bounds__(kThreads, 3) gather_kernel(const GatherParams p) {
+  constexpr int VB = NW * 4;                      // bytes per vector
+  constexpr int SLOTS = kBytesPerThread / VB;     // vectors per thread, tensor and plane
   wait_for_predecessor();
   const Ctrl* c = p.ctrl;
   if (c->abort || !c->has_dyn) return;
@@ -31,37 +40,43 @@ __global__ void __launch_bounds__(kThreads, 4) gather_kernel(const GatherParams 
   if (k <= 0) return;
   const int64_t common = c->common_len;
   const int first_dyn = c->first_dyn;
-  const int rows_per_item = (kThreads * kSlots) / p.vpr;
+  const int vpr = p.row_bytes / VB;               // vectors per row (<= kThreads: rows are at most 4 KiB)
+  const int rows_per_slot = kThreads / vpr;
+  const int rows_per_item = SLOTS * rows_per_slot;
+  const int shift = vpr >= SLOTS ? vpr / SLOTS : 1;
   const int nblk = (k + rows_per_item - 1) / rows_per_item;
   int ranges = (int)gridDim.x / nblk;
   if (ranges < 1) ranges = 1;
   if (ranges > p.n_planes) ranges = p.n_planes;
   const int ppr = (p.n_planes + ranges - 1) / ranges;
   const int items = nblk * ranges;
-  const int ppv = p.dtype == DCP_BF16 ? 4 : 2;  // rotary pairs per 16-byte vector
+  const int ppv = p.dtype == DCP_BF16 ? VB / 4 : VB / 8;   // rotary pairs per vector
   const int temporal_vecs = (p.n_t + ppv - 1) / ppv;
+  const int row_in_slot = threadIdx.x / vpr, lane_in_row = threadIdx.x - row_in_slot * vpr;
+  const int64_t src_slot = p.src_row0 * (int64_t)p.row_bytes;
 
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int jb = it % nblk, r = it / nblk;
     const int p0 = r * ppr, p1 = min(p.n_planes, p0 + ppr);
     const int j0 = jb * rows_per_item, nrows = min(rows_per_item, k - j0);
-
-    // destination vectors of the block are contiguous: vector e of the block is at dst_block + 16 e
-    const int64_t src_slot = p.src_row0 * (int64_t)p.row_bytes;
     const int64_t dst_block = (p.dst_row0 + common + j0) * (int64_t)p.row_bytes;
-    int src_rel[kSlots];  // offset of the slot's source vector inside the leaving chunk's rows, -1 if unused
-    int rot[kSlots];      // frame (inside the chunk) whose table turns this key vector, -1 if it is only copied
+
+    int src_rel[SLOTS];  // source vector inside the leaving chunk's rows, -1 if the slot is unused
+    int dst_rel[SLOTS];  // destination vector inside the block's contiguous destination rows
+    int rot[SLOTS];      // (frame << 16) | vector for a key vector the frame's table turns, -1 if it is only copied
 #pragma unroll
-    for (int u = 0; u < kSlots; ++u) {
-      const int e = threadIdx.x + u * kThreads;
-      const int row = e / p.vpr, vec = e - row * p.vpr;
+    for (int u = 0; u < SLOTS; ++u) {
+      const int row = u * rows_per_slot + row_in_slot;
+      const int vec = (lane_in_row + u * shift) % vpr;
       src_rel[u] = -1;
+      dst_rel[u] = 0;
       rot[u] = -1;
-      if (row < nrows) {
+      if (row_in_slot < rows_per_slot && row < nrows) {
         const int s = __ldg(p.idx + j0 + row);
         const int f = s / p.T;
-        src_rel[u] = s * p.row_bytes + vec * 16;
-        if (vec < temporal_vecs && __ldg(p.rot_g + f)) rot[u] = f;
+        src_rel[u] = s * p.row_bytes + vec * VB;
+        dst_rel[u] = row * p.row_bytes + vec * VB;
+        if (vec < temporal_vecs && __ldg(p.rot_g + f)) rot[u] = (f << 16) | vec;
         if (vec == 0 && first_dyn >= p0 && first_dyn < p1) p.hist_t[common + j0 + row] = p.evict_first_frame + f;
       }
     }
@@ -70,28 +85,23 @@ __global__ void __launch_bounds__(kThreads, 4) gather_kernel(const GatherParams 
       if (p.head_is_static && __ldg(p.head_is_static + pl)) continue;  // Streaming policy: keeps nothing
       char* kb = p.k + pl * p.plane_bytes;
       char* vb = p.v + pl * p.plane_bytes;
-      uint4 xk[kSlots], xv[kSlots];
+      Vec<NW> xk[SLOTS], xv[SLOTS];
 #pragma unroll
-      for (int u = 0; u < kSlots; ++u) {
+      for (int u = 0; u < SLOTS; ++u) {
         if (src_rel[u] >= 0) {
-          xk[u] = ld_stream(kb + src_slot + src_rel[u]);
-          xv[u] = ld_stream(vb + src_slot + src_rel[u]);
+          ld_stream(xk[u], kb + src_slot + src_rel[u]);
+          ld_stream(xv[u], vb + src_slot + src_rel[u]);
         }
       }
 #pragma unroll
-      for (int u = 0; u < kSlots; ++u) {
-        if (rot[u] >= 0) {
-          const int e = threadIdx.x + u * kThreads;
-          const int vec = e % p.vpr;
-          xk[u] = dev_rotate_vec(xk[u], p.dtype, vec * ppv, p.n_t, p.trig_g + rot[u] * p.n_t);
-        }
-      }
+      for (int u = 0; u < SLOTS; ++u)
+        if (rot[u] >= 0)
+          dev_rotate_vec(xk[u], p.dtype, (rot[u] & 0xFFFF) * ppv, p.n_t, p.trig_g + (rot[u] >> 16) * p.n_t);
 #pragma unroll
-      for (int u = 0; u < kSlots; ++u) {
+      for (int u = 0; u < SLOTS; ++u) {
         if (src_rel[u] >= 0) {
-          const int64_t d = dst_block + (int64_t)(threadIdx.x + u * kThreads) * 16;
-          st_stream(kb + d, xk[u]);
-          st_stream(vb + d, xv[u]);
+          st_stream(kb + dst_block + dst_rel[u], xk[u]);
+          st_stream(vb + dst_block + dst_rel[u], xv[u]);
         }
       }
       if (jb == 0 && threadIdx.x == 0) p.hist_len[pl] = (int32_t)(common + k);
@@ -99,12 +109,12 @@ __global__ void __launch_bounds__(kThreads, 4) gather_kernel(const GatherParams 
   }
 }
 
-}  // namespace
-
-cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch) {
+template <int NW>
+cudaError_t launch_gather_w(const GatherParams& p, cudaStream_t s, bool overlap_launch) {
   static int blocks_per_sm = 0;
   if (!blocks_per_sm) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, gather_kernel, kThreads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, gather_kernel<NW>, kThreads, 0) !=
+            cudaSuccess ||
         blocks_per_sm < 1)
       blocks_per_sm = 1;
   }
@@ -118,7 +128,13 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_la
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_launch ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gather_kernel, p);
+  return cudaLaunchKernelEx(&cfg, gather_kernel<NW>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch) {
+  return p.vb == 32 ? launch_gather_w<8>(p, s, overlap_launch) : launch_gather_w<4>(p, s, overlap_launch);
 }
 
 }  // namespace dcp
