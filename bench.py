@@ -302,6 +302,175 @@ def run_gpu(w, steps: int, warmup: int, world: int, rank: int, local: int, clock
     return res
 
 
+# ------------------------------------------------------------------------------------------ the other workloads
+class DeviceRollout:
+    """A device cache taken through a workload's eviction schedule by the library itself: each newly generated
+    chunk's K/V is written on the device by the seeded generator and its score inputs staged (untimed), then the prune
+    step runs.  Used for the workloads whose history matters (mid eviction, head-specialised prefix pass, rollout)."""
+
+    def __init__(self, w, head_is_static=None):
+        import torch
+
+        import autoregressive_video_diffusion_gb300 as dcp
+        from synth import workloads as W
+        self.w, self.dcp, self.W, self.torch = w, dcp, W, torch
+        self.stream = torch.cuda.current_stream()
+        self.cache = dcp.KVCache(w.L, w.H, w.D, w.dtype, w.cap, w.hist_cap)
+        s = self.stream.cuda_stream
+        W.fill_device_history_canary(self.cache.k.data_ptr(), self.cache.v.data_ptr(), w, s)
+        W.fill_device_chunks(self.cache.k.data_ptr(), self.cache.v.data_ptr(), w, list(range(w.sink_chunks)), s)
+        self.placed = set(range(w.sink_chunks))
+        self.cfg = dcp.Config(gamma=w.gamma, keep_rule=0, sink_chunks=w.sink_chunks, window_chunks=w.window_chunks,
+                              tokens_per_frame=w.tokens_per_frame, frames_per_chunk=w.frames_per_chunk,
+                              n_temporal_pairs=w.n_temporal_pairs, rope_base=w.rope_base, g_recent_R=w.R,
+                              g_span_S=w.S, g_mode=w.g_mode, max_frames=w.max_frames)
+        self.ws = dcp.new_workspace(dcp.dcp_workspace_size(self.cache, self.cfg))
+        self.static = head_is_static
+        self.hs = None if head_is_static is None else torch.from_numpy(head_is_static).cuda()
+        self.n_dyn = w.n_planes if head_is_static is None else int((head_is_static == 0).sum())
+        self.kept = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.drain_buf = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
+        self.inputs = {}
+
+    def prepare(self, c):
+        """Write the chunks resident when chunk c leaves, and stage c's score inputs on the device (untimed)."""
+        new = [cc for cc in self.w.resident_window(c) if cc not in self.placed]
+        self.W.fill_device_chunks(self.cache.k.data_ptr(), self.cache.v.data_ptr(), self.w, new,
+                                  self.stream.cuda_stream)
+        self.placed |= set(new)
+        x0, xr = self.w.score_inputs(c)
+        self.inputs[c] = (self.torch.from_numpy(x0).cuda(), self.torch.from_numpy(xr).cuda())
+
+    def step(self, c, q0_prev, q0):
+        w = self.w
+        x0, xr = self.inputs[c]
+        self.dcp.dcp_prune_step(self.cache, self.cfg, x0, xr, w.slot_of(c), w.first_frame(c), q0_prev, q0, self.hs,
+                                self.kept, None, self.ws)
+
+    def timed_step(self, c, q0_prev, q0) -> float:
+        """One prune step between CUDA events on the stream, after an L2 flush; returns ms."""
+        torch = self.torch
+        self.flush_buf.fill_(1)
+        self.drain_sum = self.drain_buf.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(self.stream)
+        self.step(c, q0_prev, q0)
+        b.record(self.stream)
+        b.synchronize()
+        return a.elapsed_time(b)
+
+    def rows_rephased(self, q0_prev, q0, hist_len_sum) -> int:
+        """History rows whose key phase moves: every history row once the span compresses (history frames are all
+        older than the dense window, so they all lie in g's linear part), none while g is the identity."""
+        w = self.w
+        T_s = w.sink_chunks * w.F
+        end = w.S if w.g_mode == 0 else w.R + w.S
+        moves = q0 != q0_prev and (q0 - T_s > end or q0_prev - T_s > end)
+        return hist_len_sum if moves else 0
+
+    def check(self):
+        st = self.dcp.dcp_get_status(self.cache.status)
+        if st != self.dcp.DCP_OK:
+            raise RuntimeError(f"{self.w.name}: prune step reported {self.dcp.dcp_status_string(st)}")
+
+
+def run_last_eviction(w, reps: int):
+    """History built by the library over the earlier evictions; the last eviction timed `reps` times, restoring the
+    history lengths, frames and key rows between repetitions (untimed)."""
+    import torch
+    r = DeviceRollout(w)
+    ev = w.evictions()
+    for c, q0p, q0 in ev[:-1]:
+        r.prepare(c)
+        r.step(c, q0p, q0)
+    c, q0p, q0 = ev[-1]
+    r.prepare(c)
+    H0 = w.sink_rows
+    hl0, ht0 = r.cache.hist_len.clone(), r.cache.hist_t.clone()
+    khist0 = r.cache.k[:, :, H0:H0 + w.hist_cap].clone()
+    hist_sum = int(hl0.sum().item())
+    times = []
+    for _ in range(reps):
+        r.cache.hist_len.copy_(hl0)
+        r.cache.hist_t.copy_(ht0)
+        r.cache.k[:, :, H0:H0 + w.hist_cap].copy_(khist0)
+        times.append(r.timed_step(c, q0p, q0))
+    r.check()
+    k = int(r.kept.item())
+    ms = float(np.median(times))
+    nbytes = w.algorithmic_bytes(k, r.n_dyn, r.rows_rephased(q0p, q0, hist_sum))
+    out = {"workload": w.name, "kept": k, "history_rows_before": int(hl0[0].item()), "q0_prev": q0p, "q0": q0,
+           "us_per_step": ms * 1e3, "algorithmic_bytes": nbytes, "GB_per_s": nbytes / (ms * 1e-3) / 1e9, "reps": reps}
+    del r, khist0
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_head_specialised(w, reps: int):
+    """Prefix pass with 20 static heads per layer: both evictions of the pass, each timed; `reps` passes."""
+    import torch
+    per = []
+    for _ in range(reps):
+        r = DeviceRollout(w, w.head_is_static())
+        row = []
+        for c, q0p, q0 in w.evictions():
+            r.prepare(c)
+            hist_sum = int(r.cache.hist_len.sum().item())
+            ms = r.timed_step(c, q0p, q0)
+            k = int(r.kept.item())
+            nbytes = w.algorithmic_bytes(k, r.n_dyn, r.rows_rephased(q0p, q0, hist_sum))
+            row.append((ms, k, nbytes))
+        r.check()
+        per.append(row)
+        del r
+        torch.cuda.empty_cache()
+    out = {"workload": w.name, "dynamic_planes": int((w.head_is_static() == 0).sum()), "evictions": []}
+    for i, (c, q0p, q0) in enumerate(w.evictions()):
+        ms = float(np.median([p[i][0] for p in per]))
+        k, nbytes = per[0][i][1], per[0][i][2]
+        out["evictions"].append({"chunk": c, "q0": q0, "kept": k, "us_per_step": ms * 1e3,
+                                 "GB_per_s": nbytes / (ms * 1e-3) / 1e9})
+    return out
+
+
+def run_rollout(w):
+    """The minute-long rollout: every chunk generated in turn, a prune step after each one that leaves the window;
+    per-step times, and the cumulative PR against FullKV kept by the library's host counter."""
+    import torch
+
+    import autoregressive_video_diffusion_gb300 as dcp
+    r = DeviceRollout(w)
+    pr = dcp.DcpPrCounter(0, 0)
+    ev = {c: (q0p, q0) for c, q0p, q0 in w.evictions()}
+    steps = []
+    for i in range(1, w.rollout_chunks):
+        hist_sum = int(r.cache.hist_len.sum().item())
+        window = min(w.window_chunks, max(0, i - w.sink_chunks)) * w.C
+        dcp.dcp_pr_add_chunk(pr, w.n_planes, hist_sum, min(w.sink_chunks, i) * w.C, window, i * w.C)
+        c = i - w.window_chunks            # the chunk that leaves once chunk i is generated
+        if c in ev:
+            q0p, q0 = ev[c]
+            r.prepare(c)
+            ms = r.timed_step(c, q0p, q0)
+            k = int(r.kept.item())
+            nbytes = w.algorithmic_bytes(k, r.n_dyn, r.rows_rephased(q0p, q0, hist_sum))
+            steps.append((ms, nbytes, k, hist_sum // w.n_planes))
+    r.check()
+    ms = np.array([s[0] for s in steps])
+    nb = np.array([s[1] for s in steps], dtype=np.float64)
+    out = {"workload": w.name, "prune_steps": len(steps), "mean_us_per_step": float(ms.mean() * 1e3),
+           "median_us_per_step": float(np.median(ms) * 1e3), "max_us_per_step": float(ms.max() * 1e3),
+           "last10_mean_us": float(ms[-10:].mean() * 1e3), "GB_per_s": float(nb.sum() / (ms.sum() * 1e-3) / 1e9),
+           "last10_GB_per_s": float(nb[-10:].sum() / (ms[-10:].sum() * 1e-3) / 1e9),
+           "final_history_rows": int(r.cache.hist_len[0].item()), "cumulative_PR": dcp.dcp_pr_value(pr),
+           "kept_fraction_mean": float(np.mean([s[2] for s in steps]) / w.C),
+           "curve_us": [round(float(x) * 1e3, 1) for x in ms]}
+    del r
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------------------------------ CPU oracle (baseline)
 class OracleSample:
     """The CPU oracle's prune step on a bounded sample of the workload: the whole score / threshold / index scan of
@@ -419,6 +588,11 @@ def main():
             "us_per_step": r2["ms_max"] * 1e3, "GB_per_s": r2["alg_bytes"] / (r2["ms_max"] * 1e-3) / 1e9,
             "gather_us": r2["gather_ms"] * 1e3,
             "gather_GB_per_s": r2["gather_bytes"] / (r2["gather_ms"] * 1e-3) / 1e9}
+        from synth.workloads import HS_PREFIX, MID, ROLLOUT, TINY
+        extra["tiny_fp32_single_prune"] = run_last_eviction(TINY, reps=20)
+        extra["mid_bf16_single_eviction"] = run_last_eviction(MID, reps=20)
+        extra["head_specialised_prefix"] = run_head_specialised(HS_PREFIX, reps=3)
+        extra["minute_rollout_gqa8"] = run_rollout(ROLLOUT)
     if rank != 0:
         return
     peak, peak_kind = _peaks()
