@@ -230,6 +230,31 @@ __device__ __forceinline__ void dev_rotate_vec(Vec<NW>& x, int dtype, int p0, in
   }
 }
 
+// Same turn with the vector's table entries already in registers: tr[i] belongs to pair p0 + i.
+template <int NW>
+__device__ __forceinline__ void dev_rotate_vec_regs(Vec<NW>& x, int dtype, int p0, int n_t, const float4 (&tr)[NW]) {
+  if (dtype == DCP_BF16) {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      if (p0 + i < n_t) {
+        float oa, ob;
+        dev_rotate(bf16lo(x.w[i]), bf16hi(x.w[i]), tr[i], oa, ob);
+        x.w[i] = pack_bf16x2(oa, ob);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW / 2; ++i) {
+      if (p0 + i < n_t) {
+        float oa, ob;
+        dev_rotate(__uint_as_float(x.w[2 * i]), __uint_as_float(x.w[2 * i + 1]), tr[i], oa, ob);
+        x.w[2 * i] = __float_as_uint(oa);
+        x.w[2 * i + 1] = __float_as_uint(ob);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
 }
@@ -267,15 +292,30 @@ __device__ __forceinline__ void st_stream(void* p, const Vec<8>& v) {
                : "memory");
 }
 
-// In-place (read-modify-write) accesses of the re-index kernel: plain cached loads and stores.
-template <int NW>
-__device__ __forceinline__ void ld_plain(Vec<NW>& v, const void* p) {
-  v = *reinterpret_cast<const Vec<NW>*>(p);
+// In-place (read-modify-write) accesses of the re-index kernel: plain cached loads and stores, written out as single
+// vector instructions (a struct copy of Vec would be split into 32-bit accesses: one L2 request per word).
+__device__ __forceinline__ void ld_plain(Vec<4>& v, const void* p) {
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+               : "l"(p));
 }
 
-template <int NW>
-__device__ __forceinline__ void st_plain(void* p, const Vec<NW>& v) {
-  *reinterpret_cast<Vec<NW>*>(p) = v;
+__device__ __forceinline__ void ld_plain(Vec<8>& v, const void* p) {
+  asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+                 "=r"(v.w[6]), "=r"(v.w[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void st_plain(void* p, const Vec<4>& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+               : "memory");
+}
+
+__device__ __forceinline__ void st_plain(void* p, const Vec<8>& v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
+               "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+               : "memory");
 }
 
 #endif  // __CUDACC__

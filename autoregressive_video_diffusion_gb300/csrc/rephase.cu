@@ -8,20 +8,23 @@
 //
 // Only the vectors of a row that hold temporal pairs are read and written (for bf16, D = 128 and n_t = 22 that is
 // the first 96 bytes of each 256-byte row: three 32-byte vectors); values and the other key dims are never touched.
-// Plane streaming as in the gather: an item is (block of history rows, range of planes); each thread owns a few fixed
-// (row, vector) pairs, looks up their frame's table row once, and walks the planes of its range.  Rows whose frame
-// does not move, and rows past a plane's own history length, are skipped.  The kernel runs before the gather of the
-// same step, so hist_len still holds the lengths before the step.
+// Plane streaming as in the gather: an item is (block of history rows, range of planes).  Each thread owns one
+// (row, vector) of the block; the cos/sin entries of that vector's pairs depend only on the row's frame, so they are
+// loaded into registers once per item and reused for every plane.  Planes are taken four at a time, so four
+// independent loads are in flight per thread.  Rows whose frame does not move, and rows past a plane's own history
+// length, are skipped.  The kernel runs before the gather of the same step, so hist_len still holds the lengths
+// before the step.
 #include "dcp_internal.cuh"
 
 namespace dcp {
 
 namespace {
 
+constexpr int kPlanesInFlight = 4;
+
 template <int NW>
 __global__ void __launch_bounds__(kThreads, 3) rephase_kernel(const RephaseParams p) {
   constexpr int VB = NW * 4;
-  constexpr int SLOTS = kBytesPerThread / VB;
   wait_for_predecessor();
   allow_dependents();
   const Ctrl* c = p.ctrl;
@@ -29,58 +32,54 @@ __global__ void __launch_bounds__(kThreads, 3) rephase_kernel(const RephaseParam
   const int rp_max = c->rp_max;
   if (rp_max <= 0 || p.nvt <= 0) return;
   const int ppv = p.dtype == DCP_BF16 ? VB / 4 : VB / 8;
-  const int rows_per_item = (kThreads * SLOTS) / p.nvt;
+  const int rows_per_item = kThreads / p.nvt;  // nvt <= kThreads: rows are at most 4 KiB
   const int nblk = (rp_max + rows_per_item - 1) / rows_per_item;
   int ranges = (int)gridDim.x / nblk;
   if (ranges < 1) ranges = 1;
   if (ranges > p.n_planes) ranges = p.n_planes;
   const int ppr = (p.n_planes + ranges - 1) / ranges;
   const int items = nblk * ranges;
+  const int row_in_item = threadIdx.x / p.nvt, vec = threadIdx.x - row_in_item * p.nvt;
+  const int64_t hist0 = p.hist_row0 * (int64_t)p.row_bytes;
 
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int jb = it % nblk, r = it / nblk;
     const int p0 = r * ppr, p1 = min(p.n_planes, p0 + ppr);
-    const int j0 = jb * rows_per_item;
+    const int row = jb * rows_per_item + row_in_item;
 
-    int off[SLOTS];       // offset of the slot's vector from the first history row, -1 if it does not turn
-    int row_of[SLOTS], vec_of[SLOTS];
-    const float4* trig[SLOTS];
-    bool any = false;
+    bool live = false;
+    float4 tr[NW];
 #pragma unroll
-    for (int u = 0; u < SLOTS; ++u) {
-      const int e = threadIdx.x + u * kThreads;
-      const int row = e / p.nvt, vec = e - row * p.nvt;
-      row_of[u] = j0 + row;
-      vec_of[u] = vec;
-      off[u] = -1;
-      trig[u] = p.trig_h;
-      if (row < rows_per_item && j0 + row < rp_max) {
-        const int t = __ldg(p.hist_t + j0 + row);
-        if (t < p.h_lo || t >= p.h_hi) {
-          set_status(p.status, DCP_EDEVICE);  // a history frame outside the table: corrupt hist_t, leave the row
-        } else if (__ldg(p.rot_h + t)) {
-          trig[u] = p.trig_h + (int64_t)t * p.n_t;
-          off[u] = (j0 + row) * p.row_bytes + vec * VB;
-        }
+    for (int i = 0; i < NW; ++i) tr[i] = make_float4(1.f, 0.f, 0.f, 0.f);
+    if (row_in_item < rows_per_item && row < rp_max) {
+      const int t = __ldg(p.hist_t + row);
+      if (t < p.h_lo || t >= p.h_hi) {
+        set_status(p.status, DCP_EDEVICE);  // a history frame outside the table: corrupt hist_t, leave the row
+      } else if (__ldg(p.rot_h + t)) {
+        live = true;
+        const float4* tt = p.trig_h + (int64_t)t * p.n_t + vec * ppv;
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+          if (i < ppv && vec * ppv + i < p.n_t) tr[i] = __ldg(tt + i);
       }
-      any |= off[u] >= 0;
     }
-    if (!__syncthreads_or(any)) continue;
+    if (!__syncthreads_or(live)) continue;
+    const int off = row * p.row_bytes + vec * VB;
 
-    const int64_t hist0 = p.hist_row0 * (int64_t)p.row_bytes;
-    for (int pl = p0; pl < p1; ++pl) {
-      const int len = __ldg(p.hist_len + pl);
-      if (len <= j0) continue;
-      char* kb = p.k + pl * p.plane_bytes + hist0;
-      Vec<NW> x[SLOTS];
+    for (int pl = p0; pl < p1; pl += kPlanesInFlight) {
+      Vec<NW> x[kPlanesInFlight];
+      bool go[kPlanesInFlight];
 #pragma unroll
-      for (int u = 0; u < SLOTS; ++u)
-        if (off[u] >= 0 && row_of[u] < len) ld_plain(x[u], kb + off[u]);
+      for (int q = 0; q < kPlanesInFlight; ++q) {
+        const int plq = pl + q;
+        go[q] = live && plq < p1 && row < __ldg(p.hist_len + min(plq, p1 - 1));
+        if (go[q]) ld_plain(x[q], p.k + plq * p.plane_bytes + hist0 + off);
+      }
 #pragma unroll
-      for (int u = 0; u < SLOTS; ++u) {
-        if (off[u] >= 0 && row_of[u] < len) {
-          dev_rotate_vec(x[u], p.dtype, vec_of[u] * ppv, p.n_t, trig[u]);
-          st_plain(kb + off[u], x[u]);
+      for (int q = 0; q < kPlanesInFlight; ++q) {
+        if (go[q]) {
+          dev_rotate_vec_regs(x[q], p.dtype, vec * ppv, p.n_t, tr);
+          st_plain(p.k + (pl + q) * p.plane_bytes + hist0 + off, x[q]);
         }
       }
     }
