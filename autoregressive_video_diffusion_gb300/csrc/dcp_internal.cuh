@@ -161,20 +161,27 @@ __device__ __forceinline__ double dev_phase(double t, double q0, double T_s, dou
   return __dsub_rn(q0, dev_g(__dsub_rn(q0, t), __dsub_rn(q0, T_s), R, S, mode));
 }
 
-// cos/sin of an angle as unevaluated float pairs (hi + lo, ~48 significant bits): {c_hi, c_lo, s_hi, s_lo}.
+// A double rounded to 16 significant bits, as a float (round half away from zero on the dropped 8 bits).
+__device__ __forceinline__ float round_to_16_bits(double x) {
+  const uint32_t u = __float_as_uint(__double2float_rn(x));
+  if ((u & 0x7F800000u) == 0x7F800000u) return __uint_as_float(u);
+  return __uint_as_float((u + 0x80u) & 0xFFFFFF00u);
+}
+
+// cos/sin of an angle as unevaluated pairs {c_hi, c_lo, s_hi, s_lo}: the high part has 16 significant bits (so its
+// product with a bf16 value, 8 bits, is exact in fp32), the low part is the fp32 rounding of the rest: ~40 bits in all.
 __device__ __forceinline__ float4 dev_trig_entry(double phi) {
   double s, c;
   sincos(phi, &s, &c);
-  float chi = __double2float_rn(c), shi = __double2float_rn(s);
+  const float chi = round_to_16_bits(c), shi = round_to_16_bits(s);
   return make_float4(chi, __double2float_rn(__dsub_rn(c, (double)chi)), shi,
                      __double2float_rn(__dsub_rn(s, (double)shi)));
 }
 
-// Rotate one pair (a, b) by the angle whose cos/sin pairs are in t:
+// Rotate one pair (a, b) of fp32 values by the angle whose cos/sin pairs are in t:
 //   out_a = a*c - b*s, out_b = a*s + b*c.
-// The rounding error of the b-products is recovered exactly with an fma and the low parts of cos/sin are added,
-// so the result carries ~2^-23 relative error plus ~2^-47 (|a| + |b|) absolute error: rounding it to bf16 gives
-// the correctly rounded value or its neighbour, never further.
+// The rounding error of the b-products is recovered exactly with an fma and the low parts of cos/sin are added, so
+// the result carries ~2^-23 relative error plus ~2^-38 (|a| + |b|) absolute error.
 __device__ __forceinline__ void dev_rotate(float a, float b, const float4 t, float& oa, float& ob) {
   float q0 = __fmul_rn(b, t.z);
   float e0 = __fmaf_rn(b, t.z, -q0);
@@ -186,6 +193,14 @@ __device__ __forceinline__ void dev_rotate(float a, float b, const float4 t, flo
   float r1 = __fmaf_rn(a, t.z, q1);
   float k1 = __fmaf_rn(a, t.w, __fmul_rn(b, t.y));
   ob = __fadd_rn(r1, __fadd_rn(k1, e1));
+}
+
+// The same turn for a pair read from bf16 storage (8 significant bits): a * c_hi and b * s_hi are exact in fp32
+// (8 + 16 bits), so one fma rounds their difference once and the low-part products complete it.  Same error bound
+// as dev_rotate: rounding the result to bf16 gives the correctly rounded value or its neighbour, never further.
+__device__ __forceinline__ void dev_rotate_bf16in(float a, float b, const float4 t, float& oa, float& ob) {
+  oa = __fadd_rn(__fmaf_rn(a, t.x, -__fmul_rn(b, t.z)), __fmaf_rn(a, t.y, -__fmul_rn(b, t.w)));
+  ob = __fadd_rn(__fmaf_rn(a, t.z, __fmul_rn(b, t.x)), __fmaf_rn(a, t.w, __fmul_rn(b, t.y)));
 }
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -212,7 +227,7 @@ __device__ __forceinline__ void dev_rotate_vec(Vec<NW>& x, int dtype, int p0, in
       const int p = p0 + i;
       if (p < n_t) {
         float oa, ob;
-        dev_rotate(bf16lo(x.w[i]), bf16hi(x.w[i]), trig[p], oa, ob);
+        dev_rotate_bf16in(bf16lo(x.w[i]), bf16hi(x.w[i]), trig[p], oa, ob);
         x.w[i] = pack_bf16x2(oa, ob);
       }
     }
@@ -238,7 +253,7 @@ __device__ __forceinline__ void dev_rotate_vec_regs(Vec<NW>& x, int dtype, int p
     for (int i = 0; i < NW; ++i) {
       if (p0 + i < n_t) {
         float oa, ob;
-        dev_rotate(bf16lo(x.w[i]), bf16hi(x.w[i]), tr[i], oa, ob);
+        dev_rotate_bf16in(bf16lo(x.w[i]), bf16hi(x.w[i]), tr[i], oa, ob);
         x.w[i] = pack_bf16x2(oa, ob);
       }
     }

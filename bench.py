@@ -471,6 +471,64 @@ def run_rollout(w):
     return out
 
 
+def run_entry_case(case: str, steps: int, warmup: int):
+    """Single entry points on their own (one GPU), for per-kernel measurement and profiling captures:
+    reindex: dcp_rope_reindex of a bf16 cache of 64 planes x 90,000 history rows (frames 4-219, ~417 rows per frame,
+             D 128, n_t 22) moved from q0 220 to 224 (then 224 -> 228, ...); algorithmic bytes 2 x 88 B per row.
+    score:   dcp_score_mask of the full-depth workload's 6240 x 64 score inputs; algorithmic bytes 2 x 6240 x 64 x 4."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import autoregressive_video_diffusion_gb300 as dcp
+    from synth.workloads import FULL
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    drain = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
+    if case == "reindex":
+        L, H, D, C, hist_cap, rows = 8, 8, 128, 6240, 100000, 90000
+        cache = dcp.KVCache(L, H, D, dcp.DCP_BF16, C + hist_cap + 4 * C, hist_cap)
+        cache.k.normal_(generator=torch.Generator(device="cuda").manual_seed(1234))
+        cache.v.zero_()
+        cache.hist_len.fill_(rows)
+        frames = (4 + np.arange(rows) * 216 // rows).astype(np.int32)
+        cache.hist_t[:rows].copy_(torch.from_numpy(frames))
+        cfg = dcp.Config(max_frames=1024)
+        ws = dcp.new_workspace(dcp.dcp_workspace_size(cache, cfg))
+
+        def call(i):
+            dcp.dcp_rope_reindex(cache, cfg, 220 + 4 * i, 224 + 4 * i, ws)
+        nbytes = L * H * rows * 2 * 88
+        status = cache.status
+    else:
+        c = FULL.evictions()[-1][0]
+        x0, xr = (torch.from_numpy(a).cuda() for a in FULL.score_inputs(c))
+        n = FULL.C
+        ws = dcp.new_workspace(dcp.dcp_score_workspace_size(n))
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kept = torch.zeros(1, dtype=torch.int32, device="cuda")
+        idx = torch.empty(n, dtype=torch.int32, device="cuda")
+
+        def call(i):
+            dcp.dcp_score_mask(x0, xr, FULL.gamma, 0, None, None, idx, kept, status, ws)
+        nbytes = 2 * n * FULL.d * 4
+    for i in range(warmup):
+        call(i)
+    times = []
+    for i in range(steps):
+        flush.fill_(1)
+        _ = drain.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call(warmup + i)
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    st = dcp.dcp_get_status(status)
+    ms = float(np.median(times))
+    print(json.dumps({"case": case, "us_per_call": ms * 1e3, "algorithmic_bytes": nbytes,
+                      "GB_per_s": nbytes / (ms * 1e-3) / 1e9, "steps": steps, "status": dcp.dcp_status_string(st)}))
+
+
 # ------------------------------------------------------------------------------------------ CPU oracle (baseline)
 class OracleSample:
     """The CPU oracle's prune step on a bounded sample of the workload: the whole score / threshold / index scan of
@@ -534,9 +592,15 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: the same workload with fewer layers (a few GB on the device)")
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before the timed region")
+    ap.add_argument("--case", default="step", choices=["step", "reindex", "score"],
+                    help="step: the prune step (default); reindex: dcp_rope_reindex of a 64-plane cache with 90,000 "
+                         "history rows per plane; score: dcp_score_mask of one full-depth chunk")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.case != "step":
+        run_entry_case(args.case, args.steps, args.warmup)
+        return
 
     from synth.workloads import FULL, FULL_ROTATED, scaled
     w = FULL if args.layers <= 0 else scaled(FULL, L=args.layers, name=f"{FULL.name}_L{args.layers}")
