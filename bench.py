@@ -34,6 +34,22 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
+# DRAM bytes (read + write) of one full-depth gather launch from the ncu capture summarised in
+# profiles/gather_kernel_full_depth_dram.md.  They describe the kernel sources they were taken on: when the hash of
+# those sources differs, the bench reports no traffic figure.
+GATHER_TRAFFIC_BYTES = 1_503_369_472
+GATHER_TRAFFIC_SOURCES_SHA256 = "ea9d1471de9f1b23e49bc697a104e89c37da4362fae9dcb21be2492277e411a3"
+
+
+def _gather_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gather.cu", "dcp_internal.cuh"):
+        with open(os.path.join(ROOT, "autoregressive_video_diffusion_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return GATHER_TRAFFIC_BYTES if h.hexdigest() == GATHER_TRAFFIC_SOURCES_SHA256 else None
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -675,7 +691,9 @@ def main():
         "pct_of_nominal_hbm": 100.0 * (value / world) / NOMINAL_HBM_GBS,
         "pct_of_measured_hbm": 100.0 * (value / world) / peak,
         "roofline": {"bound": "hbm", "kernel": "gather_kernel", "achieved": gather_gbs, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": gather_gbs / peak, "traffic": None},
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": gather_gbs / peak,
+                     "traffic": _gather_traffic() if w is FULL else None,
+                     "algorithmic_bytes_per_launch": res["gather_bytes"]},
         "phases_us": {"scan": res["scan_ms"] * 1e3, "gather": res["gather_ms"] * 1e3,
                       "note": "per-kernel events from a second loop of the same steps"},
         "gpu_launches": res["launches"],
