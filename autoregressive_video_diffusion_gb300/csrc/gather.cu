@@ -27,10 +27,12 @@ namespace dcp {
 
 namespace {
 
-// 3 CTAs per SM (up to 85 registers): the 4-CTA cap spills the rotation temporaries (measured: equal speed on
-// copies, 5 us slower on a full-depth step whose keys all turn).
+// 2 CTAs per SM (up to 128 registers) so that two planes' vectors fit in registers: the software pipeline keeps the
+// next plane's loads in flight while the current plane is turned and stored (measured on the full-depth step:
+// 248.5 us vs 253.2 us without the pipeline at 3 CTAs/SM; 259.2 us vs 269.9 us when every key turns; at 3 CTAs/SM
+// the pipelined form spills).
 template <int NW>
-__global__ void __launch_bounds__(kThreads, 3) gather_kernel(const GatherParams p) {
+__global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams p) {
   constexpr int VB = NW * 4;                      // bytes per vector
   constexpr int SLOTS = kBytesPerThread / VB;     // vectors per thread, tensor and plane
   wait_for_predecessor();
@@ -81,30 +83,51 @@ __global__ void __launch_bounds__(kThreads, 3) gather_kernel(const GatherParams 
       }
     }
 
-    for (int pl = p0; pl < p1; ++pl) {
-      if (p.head_is_static && __ldg(p.head_is_static + pl)) continue;  // Streaming policy: keeps nothing
-      char* kb = p.k + pl * p.plane_bytes;
-      char* vb = p.v + pl * p.plane_bytes;
-      Vec<NW> xk[SLOTS], xv[SLOTS];
+    // software pipeline over the planes: the next receiving plane's loads are in flight while this one is turned
+    // and stored
+    auto receives = [&](int pl) { return !(p.head_is_static && __ldg(p.head_is_static + pl)); };
+    int pl = p0;
+    while (pl < p1 && !receives(pl)) ++pl;
+    Vec<NW> ck[SLOTS], cv[SLOTS], nk[SLOTS], nv[SLOTS];
+    if (pl < p1) {
 #pragma unroll
-      for (int u = 0; u < SLOTS; ++u) {
+      for (int u = 0; u < SLOTS; ++u)
         if (src_rel[u] >= 0) {
-          ld_stream(xk[u], kb + src_slot + src_rel[u]);
-          ld_stream(xv[u], vb + src_slot + src_rel[u]);
+          ld_stream(ck[u], p.k + pl * p.plane_bytes + src_slot + src_rel[u]);
+          ld_stream(cv[u], p.v + pl * p.plane_bytes + src_slot + src_rel[u]);
         }
+    }
+    while (pl < p1) {
+      int nx = pl + 1;
+      while (nx < p1 && !receives(nx)) ++nx;
+      if (nx < p1) {
+#pragma unroll
+        for (int u = 0; u < SLOTS; ++u)
+          if (src_rel[u] >= 0) {
+            ld_stream(nk[u], p.k + nx * p.plane_bytes + src_slot + src_rel[u]);
+            ld_stream(nv[u], p.v + nx * p.plane_bytes + src_slot + src_rel[u]);
+          }
       }
 #pragma unroll
       for (int u = 0; u < SLOTS; ++u)
         if (rot[u] >= 0)
-          dev_rotate_vec(xk[u], p.dtype, (rot[u] & 0xFFFF) * ppv, p.n_t, p.trig_g + (rot[u] >> 16) * p.n_t);
+          dev_rotate_vec(ck[u], p.dtype, (rot[u] & 0xFFFF) * ppv, p.n_t, p.trig_g + (rot[u] >> 16) * p.n_t);
+      char* kb = p.k + pl * p.plane_bytes;
+      char* vb = p.v + pl * p.plane_bytes;
 #pragma unroll
       for (int u = 0; u < SLOTS; ++u) {
         if (src_rel[u] >= 0) {
-          st_stream(kb + dst_block + dst_rel[u], xk[u]);
-          st_stream(vb + dst_block + dst_rel[u], xv[u]);
+          st_stream(kb + dst_block + dst_rel[u], ck[u]);
+          st_stream(vb + dst_block + dst_rel[u], cv[u]);
         }
       }
       if (jb == 0 && threadIdx.x == 0) p.hist_len[pl] = (int32_t)(common + k);
+#pragma unroll
+      for (int u = 0; u < SLOTS; ++u) {
+        ck[u] = nk[u];
+        cv[u] = nv[u];
+      }
+      pl = nx;
     }
   }
 }
