@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one full-depth gather launch from the ncu capture summarised in
 # profiles/gather_kernel_full_depth_dram.md.  They describe the kernel sources they were taken on: when the hash of
 # those sources differs, the bench reports no traffic figure.
-GATHER_TRAFFIC_BYTES = 1_503_369_472
-GATHER_TRAFFIC_SOURCES_SHA256 = "ea9d1471de9f1b23e49bc697a104e89c37da4362fae9dcb21be2492277e411a3"
+GATHER_TRAFFIC_BYTES = 1_500_011_008
+GATHER_TRAFFIC_SOURCES_SHA256 = "c90929ee4c7a38817c706c35694c9a7e2faab07cf5dfd534e8081ad5b8834434"
 
 
 def _gather_traffic():
