@@ -42,7 +42,7 @@ class OracleConfig(ctypes.Structure):
                 ("window_chunks", ctypes.c_int32), ("tokens_per_frame", ctypes.c_int32),
                 ("frames_per_chunk", ctypes.c_int32), ("n_temporal_pairs", ctypes.c_int32),
                 ("rope_base", ctypes.c_double), ("g_recent_R", ctypes.c_double), ("g_span_S", ctypes.c_double),
-                ("g_mode", ctypes.c_int32)]
+                ("g_mode", ctypes.c_int32), ("random_seed", ctypes.c_uint32)]
 
 
 _lib = None
@@ -61,6 +61,8 @@ def lib():
             "oracle_default_gamma": ([], f32),
             "oracle_score": ([vp, vp, i64, i32, vp], None),
             "oracle_keep": ([vp, i64, f32, i32, vp], None),
+            "oracle_splitmix64": ([ctypes.c_uint64, i64], ctypes.c_uint64),
+            "oracle_keep_random": ([vp, i64, f32, ctypes.c_uint64, vp], None),
             "oracle_indices": ([vp, i64, vp], i64),
             "oracle_g": ([f64, f64, f64, f64, i32], f64),
             "oracle_phase": ([f64, f64, f64, f64, f64, i32], f64),
@@ -103,11 +105,16 @@ class Cfg:
     g_recent_R: float = 12.0
     g_span_S: float = 24.0
     g_mode: int = 0
+    random_seed: int = 0
 
     def c(self) -> OracleConfig:
         return OracleConfig(self.gamma, self.keep_rule, self.sink_chunks, self.window_chunks, self.tokens_per_frame,
                             self.frames_per_chunk, self.n_temporal_pairs, self.rope_base, self.g_recent_R,
-                            self.g_span_S, self.g_mode)
+                            self.g_span_S, self.g_mode, self.random_seed)
+
+    def random_stream(self, evict_first_frame: int) -> int:
+        """The SplitMix64 stream a prune step of the Random ablation (keep_rule 2) draws from."""
+        return ((self.random_seed & 0xFFFFFFFF) << 32) | (evict_first_frame & 0xFFFFFFFF)
 
 
 class HostCache:
@@ -141,6 +148,17 @@ def score(x0hat: np.ndarray, xref: np.ndarray) -> np.ndarray:
 def keep(ell: np.ndarray, gamma: float = 0.10, keep_rule: int = 0) -> np.ndarray:
     out = np.empty(ell.shape[0], np.uint8)
     lib().oracle_keep(_p(np.ascontiguousarray(ell, np.float32)), ell.shape[0], gamma, keep_rule, _p(out))
+    return out
+
+
+def splitmix64(stream: int, i: int) -> int:
+    return lib().oracle_splitmix64(stream, i)
+
+
+def keep_random(ell: np.ndarray, gamma: float, stream: int) -> np.ndarray:
+    """Random ablation: as many tokens as ell > gamma would keep, drawn uniformly from the SplitMix64 stream."""
+    out = np.empty(ell.shape[0], np.uint8)
+    lib().oracle_keep_random(_p(np.ascontiguousarray(ell, np.float32)), ell.shape[0], gamma, stream, _p(out))
     return out
 
 

@@ -12,13 +12,15 @@
 //
 // Style: one thread, plain loops, fp64 arithmetic, one rounding to the storage type at the end of each value.
 // Readings of points the page leaves open (each listed in the design doc):
-//   * keep rule: keep when l > gamma (strict), drop otherwise; the reverse criterion is the complement.
+//   * keep rule: keep when l > gamma (strict), drop otherwise; the reverse criterion is the complement; the Random
+//     ablation keeps the same number of tokens, drawn uniformly without replacement from a SplitMix64 stream.
 //   * pair p of the temporal RoPE sub-vector occupies dims (2p, 2p+1); theta_p = base^(-p / n_t).
 //   * g(D) = D when D <= R (recent offsets) or when no compression is needed; otherwise a linear map that sends R to
 //     R and the oldest non-sink offset Dmax to the span end (mode 0: S is the total virtual span; mode 1: old offsets
 //     occupy (R, R + S]).
 //   * the sink keeps its phase; only history keys are re-phased; values and non-temporal dims are copied bitwise.
 // Parity: every function here is pinned by tests/test_oracle_pins.py (closed forms, invariants, brute force).
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -38,12 +40,14 @@ struct oracle_cache {
 
 struct oracle_config {
   float gamma;
-  int32_t keep_rule;     // 0 = keep large discrepancy (DeCoPrune), 1 = the reverse criterion
+  int32_t keep_rule;     // 0 = keep large discrepancy (DeCoPrune), 1 = the reverse criterion, 2 = Random at the
+                         // same count as rule 0
   int32_t sink_chunks, window_chunks, tokens_per_frame, frames_per_chunk;
   int32_t n_temporal_pairs;
   double rope_base;
   double g_recent_R, g_span_S;
   int32_t g_mode;        // 0: S is the total virtual span; 1: old offsets occupy (R, R + S]
+  uint32_t random_seed;  // keep_rule 2: the prune step draws from the stream (random_seed << 32) | evict_first_frame
 };
 
 enum { ORACLE_OK = 0, ORACLE_EINVAL = 1, ORACLE_ECAPACITY = 2 };
@@ -77,6 +81,30 @@ void oracle_keep(const float* ell, int64_t n, float gamma, int32_t keep_rule, ui
     bool large = ell[i] > gamma;
     mask[i] = (uint8_t)(keep_rule == 0 ? large : !large);
   }
+}
+
+// ------------------------------------------------------------------------------------------- Random ablation [limits]
+// The page's ablation compares DeCoPrune with a Random policy at the same compression ratio.  Reading: Random keeps
+// as many tokens of the chunk as the discrepancy rule would (so the PR is the same chunk by chunk), drawn uniformly
+// without replacement.  The draw: token n gets the n-th output of a SplitMix64 sequence (Steele, Lea & Flood, "Fast
+// splittable pseudorandom number generators", OOPSLA 2014) started at the stream value, and the tokens with the
+// smallest outputs are kept.  The outputs of one sequence are distinct (the state steps by an odd constant and the
+// output function is a bijection of 64-bit words), so the kept set is unique.
+uint64_t oracle_splitmix64(uint64_t stream, int64_t i) {
+  uint64_t z = stream + (uint64_t)(i + 1) * 0x9E3779B97F4A7C15ull;  // state after i + 1 steps
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+void oracle_keep_random(const float* ell, int64_t n, float gamma, uint64_t stream, uint8_t* mask) {
+  int64_t k = 0;
+  for (int64_t i = 0; i < n; ++i) k += ell[i] > gamma ? 1 : 0;
+  std::vector<std::pair<uint64_t, int64_t>> order((size_t)n);
+  for (int64_t i = 0; i < n; ++i) order[(size_t)i] = {oracle_splitmix64(stream, i), i};
+  std::sort(order.begin(), order.end());
+  for (int64_t i = 0; i < n; ++i) mask[i] = 0;
+  for (int64_t j = 0; j < k; ++j) mask[order[(size_t)j].second] = 1;
 }
 
 // ------------------------------------------------------------------------------------------- indices m [how]
@@ -241,7 +269,11 @@ int32_t oracle_prune_step(oracle_cache* c, const oracle_config* cfg, const float
   std::vector<float> ell((size_t)C);
   std::vector<uint8_t> mask((size_t)C);
   oracle_score(x0hat, xref, C, d, ell.data());
-  oracle_keep(ell.data(), C, cfg->gamma, cfg->keep_rule, mask.data());
+  if (cfg->keep_rule == 2)
+    oracle_keep_random(ell.data(), C, cfg->gamma, ((uint64_t)cfg->random_seed << 32) | (uint32_t)evict_first_frame,
+                       mask.data());
+  else
+    oracle_keep(ell.data(), C, cfg->gamma, cfg->keep_rule, mask.data());
   if (ell_out) std::memcpy(ell_out, ell.data(), sizeof(float) * (size_t)C);
   if (mask_out) std::memcpy(mask_out, mask.data(), (size_t)C);
   // the step is checked before anything moves, so a refused step leaves the cache as it was

@@ -426,3 +426,71 @@ def test_pr_tends_to_drop_fraction():
         if i - 1 >= 4:
             hist += int(p * C)
     assert abs((1 - vis / full) - (1 - p)) < 0.02
+
+
+# ------------------------------------------------------------------------------------------ Random ablation
+def test_splitmix64_published_outputs():
+    """The generator of the Random ablation reproduces the published SplitMix64 outputs for seed 1234567."""
+    for seed, i, want in _golden_lines("splitmix64.txt"):
+        assert oracle.splitmix64(int(seed), int(i)) == int(want)
+
+
+def _ell_with_k(n, k, seed):
+    rng = np.random.default_rng(seed)
+    ell = rng.uniform(0.0, 0.09, n).astype(np.float32)
+    ell[rng.choice(n, k, replace=False)] = rng.uniform(0.11, 2.0, k).astype(np.float32)
+    return ell
+
+
+@pytest.mark.parametrize("n,k", [(64, 0), (64, 64), (64, 9), (1000, 151), (6240, 947)])
+def test_random_keeps_the_discrepancy_count(n, k):
+    """Section 'premises and limits': Random is compared at the same compression ratio, so it keeps exactly as many
+    tokens as the discrepancy rule; the kept set is the k smallest generator outputs (every kept output is below every
+    dropped one), and it does not depend on which tokens have large discrepancy."""
+    ell = _ell_with_k(n, k, 7 + n + k)
+    stream = (0xC0FFEE << 32) | 17
+    m = oracle.keep_random(ell, 0.10, stream)
+    assert int(m.sum()) == k == int((ell > np.float32(0.10)).sum())
+    z = np.array([oracle.splitmix64(stream, i) for i in range(n)], dtype=np.uint64)
+    assert len(set(z.tolist())) == n
+    if 0 < k < n:
+        assert z[m == 1].max() < z[m == 0].min()
+    perm = np.random.default_rng(3).permutation(n)
+    assert np.array_equal(oracle.keep_random(ell[perm], 0.10, stream), m)
+    assert not np.array_equal(oracle.keep_random(ell, 0.10, stream + 1), m) or k in (0, n)
+
+
+def test_random_draw_is_uniform_over_subsets():
+    """A uniform draw of k of n tokens without replacement: each token is kept with probability k/n and each pair
+    with probability k(k-1)/(n(n-1)).  Checked over 3000 streams (n = 12, k = 4) within 5 standard deviations."""
+    n, k, reps = 12, 4, 3000
+    ell = _ell_with_k(n, k, 5)
+    single = np.zeros(n)
+    pair = np.zeros((n, n))
+    for r in range(reps):
+        m = oracle.keep_random(ell, 0.10, (r * 0x9E3779B1) & ((1 << 64) - 1)).astype(np.float64)
+        single += m
+        pair += np.outer(m, m)
+    p1 = k / n
+    assert np.all(np.abs(single / reps - p1) < 5 * math.sqrt(p1 * (1 - p1) / reps))
+    p2 = k * (k - 1) / (n * (n - 1))
+    off = pair[~np.eye(n, dtype=bool)] / reps
+    assert np.all(np.abs(off - p2) < 5 * math.sqrt(p2 * (1 - p2) / reps))
+
+
+def test_random_prune_step_stream():
+    """A prune step under keep_rule 2 draws from the stream (random_seed << 32) | evict_first_frame and moves the
+    same number of rows as the discrepancy rule."""
+    w = TINY
+    hc, ev = replay.state_before_last(w)
+    c, q0_prev, q0 = ev
+    cfg = replay.cfg_of(w)
+    cfg.keep_rule, cfg.random_seed = 2, 0xABCDEF
+    x0, xr = w.score_inputs(c)
+    ef = w.first_frame(c)
+    h2 = hc.copy()
+    rc, ell, mask, idx = oracle.prune_step(h2, cfg, x0, xr, w.slot_of(c), ef, q0_prev, q0)
+    assert rc == oracle.OK
+    assert np.array_equal(mask, oracle.keep_random(ell, cfg.gamma, cfg.random_stream(ef)))
+    assert len(idx) == int((ell > np.float32(cfg.gamma)).sum())
+    assert np.array_equal(idx, np.flatnonzero(mask))
