@@ -50,7 +50,7 @@ class DcpConfigC(ctypes.Structure):
                 ("frames_per_chunk", ctypes.c_int32), ("n_temporal_pairs", ctypes.c_int32),
                 ("pair_layout", ctypes.c_int32), ("rope_base", ctypes.c_double), ("g_recent_R", ctypes.c_double),
                 ("g_span_S", ctypes.c_double), ("g_mode", ctypes.c_int32), ("rephase_sink", ctypes.c_int32),
-                ("max_frames", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("max_frames", ctypes.c_int32), ("random_seed", ctypes.c_uint32)]
 
 
 class DcpPrCounter(ctypes.Structure):
@@ -63,7 +63,8 @@ _SIGS = {
     "dcp_workspace_size": ([_pc, _pg], _sz),
     "dcp_score_workspace_size": ([_i32], _sz),
     "dcp_workspace_init": ([_vp, _sz, _vp], _i32),
-    "dcp_score_mask": ([_vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "dcp_score_mask": ([_vp, _vp, _i32, _i32, _f32, _i32, ctypes.c_uint64, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                        _vp], _i32),
     "dcp_compact_layers": ([_pc, _pg, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp], _i32),
     "dcp_rope_reindex": ([_pc, _pg, _i32, _i32, _vp, _sz, _vp], _i32),
     "dcp_prune_step": ([_pc, _pg, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -132,6 +133,7 @@ class Config:
     max_frames: int = 256
     pair_layout: int = 0
     rephase_sink: int = 0
+    random_seed: int = 0
 
     @property
     def C(self) -> int:
@@ -140,7 +142,12 @@ class Config:
     def c(self) -> DcpConfigC:
         return DcpConfigC(self.gamma, self.keep_rule, self.sink_chunks, self.window_chunks, self.tokens_per_frame,
                           self.frames_per_chunk, self.n_temporal_pairs, self.pair_layout, self.rope_base,
-                          self.g_recent_R, self.g_span_S, self.g_mode, self.rephase_sink, self.max_frames, 0)
+                          self.g_recent_R, self.g_span_S, self.g_mode, self.rephase_sink, self.max_frames,
+                          self.random_seed & 0xFFFFFFFF)
+
+    def random_stream(self, evict_first_frame: int) -> int:
+        """SplitMix64 seed a prune step under keep_rule 2 draws from (as dcp_prune_step forms it)."""
+        return ((self.random_seed & 0xFFFFFFFF) << 32) | (evict_first_frame & 0xFFFFFFFF)
 
 
 class KVCache:
@@ -186,10 +193,11 @@ def new_workspace(nbytes: int, device="cuda", stream=None) -> torch.Tensor:
 
 
 def dcp_score_mask(x0hat: torch.Tensor, xref: torch.Tensor, gamma: float, keep_rule: int, ell, mask, idx, kept,
-                   status: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+                   status: torch.Tensor, ws: torch.Tensor, stream=None, random_stream: int = 0) -> None:
     n_tok, d = x0hat.shape
-    _check(lib.dcp_score_mask(_ptr(x0hat), _ptr(xref), n_tok, d, gamma, keep_rule, _ptr(ell), _ptr(mask), _ptr(idx),
-                              _ptr(kept), _ptr(status), _ptr(ws), ws.numel(), _stream(stream)), "dcp_score_mask")
+    _check(lib.dcp_score_mask(_ptr(x0hat), _ptr(xref), n_tok, d, gamma, keep_rule, random_stream, _ptr(ell),
+                              _ptr(mask), _ptr(idx), _ptr(kept), _ptr(status), _ptr(ws), ws.numel(), _stream(stream)),
+           "dcp_score_mask")
 
 
 def dcp_compact_layers(cache: KVCache, cfg: Config, evict_slot: int, evict_first_frame: int, mask: torch.Tensor,

@@ -37,14 +37,14 @@ dcp_status check_cache_cfg(const dcp_cache* c, const dcp_config* g, Derived* d) 
   const int64_t C = (int64_t)g->tokens_per_frame * g->frames_per_chunk;
   if (C > (int64_t(1) << 30)) return DCP_EINVAL;
   if (g->n_temporal_pairs < 0 || g->n_temporal_pairs > c->D / 2) return DCP_EINVAL;
-  if (g->pair_layout != 0 || g->rephase_sink != 0 || g->reserved != 0) return DCP_EINVAL;
+  if (g->pair_layout != 0 || g->rephase_sink != 0) return DCP_EINVAL;
   if (!std::isfinite(g->rope_base) || !(g->rope_base > 0.0)) return DCP_EINVAL;
   if (!std::isfinite(g->g_recent_R) || !std::isfinite(g->g_span_S)) return DCP_EINVAL;
   if (g->g_mode != 0 && g->g_mode != 1) return DCP_EINVAL;
   if (g->g_recent_R < (double)g->window_chunks * g->frames_per_chunk) return DCP_EINVAL;
   if (g->g_mode == 0 && g->g_span_S < g->g_recent_R) return DCP_EINVAL;
   if (g->g_mode == 1 && g->g_span_S < 0.0) return DCP_EINVAL;
-  if (g->keep_rule != 0 && g->keep_rule != 1) return DCP_EINVAL;
+  if (g->keep_rule < 0 || g->keep_rule > 2) return DCP_EINVAL;
   if (!std::isfinite(g->gamma)) return DCP_EINVAL;
   if (g->max_frames < 1) return DCP_EINVAL;
   if (c->hist_cap < 0 || c->hist_cap > INT32_MAX) return DCP_EINVAL;
@@ -218,10 +218,11 @@ dcp_status dcp_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 }
 
 dcp_status dcp_score_mask(const float* x0hat, const float* xref, int32_t n_tok, int32_t d, float gamma,
-                          int32_t keep_rule, float* ell_dev, uint8_t* mask_dev, int32_t* idx_dev, int32_t* kept_dev,
-                          int32_t* status_dev, void* ws, size_t ws_bytes, void* stream) {
+                          int32_t keep_rule, uint64_t random_stream, float* ell_dev, uint8_t* mask_dev,
+                          int32_t* idx_dev, int32_t* kept_dev, int32_t* status_dev, void* ws, size_t ws_bytes,
+                          void* stream) {
   if (!x0hat || !xref || !status_dev || n_tok < 1 || n_tok > (1 << 30) || d < 1 || !std::isfinite(gamma) ||
-      (keep_rule != 0 && keep_rule != 1))
+      keep_rule < 0 || keep_rule > 2)
     return DCP_EINVAL;
   if (!aligned(status_dev, 4) || (idx_dev && !aligned(idx_dev, 4)) || (ell_dev && !aligned(ell_dev, 4)) ||
       (kept_dev && !aligned(kept_dev, 4)) || !aligned(x0hat, 4) || !aligned(xref, 4))
@@ -235,6 +236,7 @@ dcp_status dcp_score_mask(const float* x0hat, const float* xref, int32_t n_tok, 
   sp.d = d;
   sp.gamma = gamma;
   sp.keep_rule = keep_rule;
+  sp.random_stream = random_stream;
   choose_tiling(d, x0hat, xref, &sp.lpt, &sp.tile);
   sp.n_tiles = (n_tok + sp.tile - 1) / sp.tile;
   sp.ell_out = ell_dev;
@@ -326,6 +328,7 @@ dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const f
   sp.want_rephase = rephase ? 1 : 0;
   sp.head_is_static = head_is_static;
   sp.evict_first_frame = evict_first_frame;
+  sp.random_stream = ((uint64_t)cfg->random_seed << 32) | (uint32_t)evict_first_frame;
   sp.g_frames = cfg->frames_per_chunk;
   sp.h_lo = d.T_s;
   sp.h_hi = rephase ? evict_first_frame : d.T_s;

@@ -65,7 +65,8 @@ struct ScanParams {
   const uint8_t* mask_in;
   int32_t n_tok, d;
   float gamma;
-  int32_t keep_rule;
+  int32_t keep_rule;       // 2 (with score inputs): the Random ablation at rule 0's count
+  uint64_t random_stream;  // its SplitMix64 seed
   int32_t tile, n_tiles, lpt;  // tokens per tile, tiles, lanes per token of the vector path (0 = warp path)
   float* ell_out;
   uint8_t* mask_out;

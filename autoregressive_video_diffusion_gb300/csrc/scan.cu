@@ -14,7 +14,8 @@
 //                (receiving planes' shortest and longest history, lowest receiving plane, longest history).
 //   final CTA    the last CTA to finish (completion counter) turns the ballot words into the ordered index list
 //                with one block-wide exclusive scan of their popcounts per 256 words, decides capacity and
-//                consistency, publishes the verdict for the kernels that follow and resets the counters.
+//                consistency, publishes the verdict for the kernels that follow and resets the counters.  Under
+//                the Random ablation (keep rule 2) it first draws the kept set (radix select, below).
 // Every step of that chain is a fixed number of dependent memory round trips; no CTA waits on another.  (A
 // decoupled look-back over 98 tiles measured 11.8 us for a 6240-token chunk on GB300, where each polling round is a
 // cross-die L2 round trip; this single-pass form removes the polling.)  The kernel lets its dependents launch early
@@ -107,12 +108,12 @@ __device__ void tile_work(const ScanParams& p, int tile_id, float* s_ell) {
     if (p.x0hat) {
       const float l = s_ell[tid];
       const bool large = l > p.gamma;
-      keep = p.keep_rule == 0 ? large : !large;
+      keep = p.keep_rule == 1 ? !large : large;  // rule 2 publishes rule 0's bits: the final CTA draws that many
       if (p.ell_out) p.ell_out[t0 + tid] = l;
     } else {
       keep = p.mask_in[t0 + tid] != 0;
     }
-    if (p.mask_out) p.mask_out[t0 + tid] = (uint8_t)keep;
+    if (p.mask_out && !(p.x0hat && p.keep_rule == 2)) p.mask_out[t0 + tid] = (uint8_t)keep;
   }
   const unsigned word = __ballot_sync(kFull, keep);
   const int w = tid >> 5;
@@ -181,14 +182,95 @@ __device__ void table_work(const ScanParams& p, int block) {
   }
 }
 
+// ------------------------------------------------------------------------------------------ Random ablation
+// Section "premises and limits" of the page compares DeCoPrune with a Random policy at the same compression ratio.
+// Keep rule 2 keeps as many tokens as the discrepancy rule would, drawn uniformly without replacement: token n gets
+// the priority z_n, the n-th output (0-based) of a SplitMix64 sequence (Steele, Lea & Flood, "Fast splittable
+// pseudorandom number generators", OOPSLA 2014) seeded with the call's stream, and the tokens with the smallest
+// priorities are kept.  The state steps by an odd constant and the output function is a bijection of 64-bit words,
+// so the priorities of one chunk are distinct and the kept set is unique.
+__device__ __forceinline__ uint64_t dev_splitmix64(uint64_t seed, uint64_t i) {
+  uint64_t z = seed + (i + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+struct Pick {          // kept set of rule 2: any && (z >> shift) <= prefix
+  uint64_t prefix;
+  int shift;
+  bool any;
+};
+
+// Radix select, most significant byte first, of the target-th smallest priority in one CTA (s_pick: kThreads + 3
+// ints).  A pass histograms the next byte of the priorities that still match the chosen prefix; the byte whose
+// bin holds the remaining rank extends the prefix.  It stops as soon as the whole bin is taken; with distinct
+// priorities that happens at the latest when one priority is left (byte 0).  The count of rule 0 comes from the
+// ballot words the tile CTAs published.
+__device__ Pick random_pick(const ScanParams& p, int n_words, int* s_warp, int* s_pick) {
+  int target = 0;  // same value in every thread
+  for (int w0 = 0; w0 < n_words; w0 += kThreads) {
+    const int wi = w0 + threadIdx.x;
+    int total = 0;
+    block_exclusive_scan(wi < n_words ? __popc(__ldcg(p.bits + wi)) : 0, s_warp, &total);
+    target += total;
+  }
+  Pick pk{0ull, 0, target > 0};
+  if (!pk.any) return pk;
+  int r = target;
+  uint64_t prefix = 0;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    s_pick[threadIdx.x] = 0;
+    __syncthreads();
+    for (int n = threadIdx.x; n < p.n_tok; n += kThreads) {
+      const uint64_t z = dev_splitmix64(p.random_stream, (uint64_t)n);
+      if (shift == 56 || (z >> (shift + 8)) == prefix) atomicAdd(&s_pick[(z >> shift) & 255], 1);
+    }
+    __syncthreads();
+    const int h = s_pick[threadIdx.x];
+    int total = 0;
+    const int below = block_exclusive_scan(h, s_warp, &total);
+    if (below < r && r <= below + h) {
+      s_pick[kThreads] = threadIdx.x;
+      s_pick[kThreads + 1] = below;
+      s_pick[kThreads + 2] = h;
+    }
+    __syncthreads();
+    const int digit = s_pick[kThreads], taken_below = s_pick[kThreads + 1], in_bin = s_pick[kThreads + 2];
+    r -= taken_below;
+    prefix = (prefix << 8) | (uint64_t)digit;
+    pk.prefix = prefix;
+    pk.shift = shift;
+    if (r == in_bin) break;
+  }
+  return pk;
+}
+
+// Ballot word wi of rule 2's kept set; also writes those tokens' mask bytes.
+__device__ unsigned random_word(const ScanParams& p, const Pick& pk, int wi) {
+  unsigned word = 0u;
+  for (int b = 0; b < 32; ++b) {
+    const int n = wi * 32 + b;
+    if (n >= p.n_tok) break;
+    const bool keep = pk.any && (dev_splitmix64(p.random_stream, (uint64_t)n) >> pk.shift) <= pk.prefix;
+    word |= (unsigned)keep << b;
+    if (p.mask_out) p.mask_out[n] = (uint8_t)keep;
+  }
+  return word;
+}
+
 // The last CTA: ballot words -> ordered index list (block scan of popcounts), then the step's verdict.
-__device__ void finalize(const ScanParams& p, int* s_warp) {
+__device__ void finalize(const ScanParams& p, int* s_warp, int* s_pick) {
   Ctrl* c = p.ctrl;
   const int n_words = p.n_tiles > 0 ? (p.n_tok + 31) >> 5 : 0;
+  const bool random = p.x0hat && p.keep_rule == 2;
+  Pick pk{0ull, 0, false};
+  if (random) pk = random_pick(p, n_words, s_warp, s_pick);
   int k = 0;  // same value in every thread
   for (int w0 = 0; w0 < n_words; w0 += kThreads) {
     const int wi = w0 + threadIdx.x;
-    unsigned word = wi < n_words ? __ldcg(p.bits + wi) : 0u;  // written by other CTAs: read through L2
+    unsigned word = 0u;
+    if (wi < n_words) word = random ? random_word(p, pk, wi) : __ldcg(p.bits + wi);  // other CTAs' words: via L2
     int total = 0;
     const int excl = block_exclusive_scan(__popc(word), s_warp, &total);
     if (p.idx_out) {
@@ -242,6 +324,7 @@ __device__ void finalize(const ScanParams& p, int* s_warp) {
 __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanParams p) {
   __shared__ float s_ell[kMaxTile];
   __shared__ int s_warp[kThreads / 32];
+  __shared__ int s_pick[kThreads + 3];
   __shared__ int s_last;
   allow_dependents();
   const int id = blockIdx.x;
@@ -258,7 +341,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanParams p) {
     if (s_last) __threadfence();
   }
   __syncthreads();
-  if (s_last) finalize(p, s_warp);
+  if (s_last) finalize(p, s_warp, s_pick);
 }
 
 }  // namespace

@@ -169,7 +169,7 @@ def job_throughput(bytes_per_rank_step: int, ms_max: float, world: int) -> float
 class FullDepthStep:
     """Device state of one eviction of a full-size workload, ready to be pruned repeatedly."""
 
-    def __init__(self, w):
+    def __init__(self, w, keep_rule: int = 0, random_seed: int = 0):
         import torch
 
         import autoregressive_video_diffusion_gb300 as dcp
@@ -182,10 +182,11 @@ class FullDepthStep:
         W.fill_device_chunks(self.cache.k.data_ptr(), self.cache.v.data_ptr(), w,
                              list(range(w.sink_chunks)) + w.resident_window(c), stream)
         W.fill_device_history_canary(self.cache.k.data_ptr(), self.cache.v.data_ptr(), w, stream)
-        self.cfg = dcp.Config(gamma=w.gamma, keep_rule=0, sink_chunks=w.sink_chunks, window_chunks=w.window_chunks,
-                              tokens_per_frame=w.tokens_per_frame, frames_per_chunk=w.frames_per_chunk,
-                              n_temporal_pairs=w.n_temporal_pairs, rope_base=w.rope_base, g_recent_R=w.R,
-                              g_span_S=w.S, g_mode=w.g_mode, max_frames=w.max_frames)
+        self.cfg = dcp.Config(gamma=w.gamma, keep_rule=keep_rule, sink_chunks=w.sink_chunks,
+                              window_chunks=w.window_chunks, tokens_per_frame=w.tokens_per_frame,
+                              frames_per_chunk=w.frames_per_chunk, n_temporal_pairs=w.n_temporal_pairs,
+                              rope_base=w.rope_base, g_recent_R=w.R, g_span_S=w.S, g_mode=w.g_mode,
+                              max_frames=w.max_frames, random_seed=random_seed)
         self.ws = dcp.new_workspace(dcp.dcp_workspace_size(self.cache, self.cfg))
         x0, xr = w.score_inputs(c)
         self.x0_host = torch.from_numpy(x0).pin_memory()
@@ -222,11 +223,11 @@ class FullDepthStep:
 
 
 def run_gpu(w, steps: int, warmup: int, world: int, rank: int, local: int, clocks: ClockSampler | None,
-            e2e_steps: int, preroll_s: float = 1.0):
+            e2e_steps: int, preroll_s: float = 1.0, keep_rule: int = 0):
     import torch
 
     import autoregressive_video_diffusion_gb300 as dcp
-    s = FullDepthStep(w)
+    s = FullDepthStep(w, keep_rule=keep_rule, random_seed=0x5EED)
     stream = torch.cuda.current_stream()
     ev_scan, ev_gather = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev_scan.record(stream)
@@ -340,10 +341,11 @@ class DeviceRollout:
         W.fill_device_history_canary(self.cache.k.data_ptr(), self.cache.v.data_ptr(), w, s)
         W.fill_device_chunks(self.cache.k.data_ptr(), self.cache.v.data_ptr(), w, list(range(w.sink_chunks)), s)
         self.placed = set(range(w.sink_chunks))
-        self.cfg = dcp.Config(gamma=w.gamma, keep_rule=0, sink_chunks=w.sink_chunks, window_chunks=w.window_chunks,
-                              tokens_per_frame=w.tokens_per_frame, frames_per_chunk=w.frames_per_chunk,
-                              n_temporal_pairs=w.n_temporal_pairs, rope_base=w.rope_base, g_recent_R=w.R,
-                              g_span_S=w.S, g_mode=w.g_mode, max_frames=w.max_frames)
+        self.cfg = dcp.Config(gamma=w.gamma, keep_rule=keep_rule, sink_chunks=w.sink_chunks,
+                              window_chunks=w.window_chunks, tokens_per_frame=w.tokens_per_frame,
+                              frames_per_chunk=w.frames_per_chunk, n_temporal_pairs=w.n_temporal_pairs,
+                              rope_base=w.rope_base, g_recent_R=w.R, g_span_S=w.S, g_mode=w.g_mode,
+                              max_frames=w.max_frames, random_seed=random_seed)
         self.ws = dcp.new_workspace(dcp.dcp_workspace_size(self.cache, self.cfg))
         self.static = head_is_static
         self.hs = None if head_is_static is None else torch.from_numpy(head_is_static).cuda()
@@ -672,6 +674,12 @@ def main():
             "us_per_step": r2["ms_max"] * 1e3, "GB_per_s": r2["alg_bytes"] / (r2["ms_max"] * 1e-3) / 1e9,
             "gather_us": r2["gather_ms"] * 1e3,
             "gather_GB_per_s": r2["gather_bytes"] / (r2["gather_ms"] * 1e-3) / 1e9}
+        r3 = run_gpu(FULL, max(5, args.steps // 2), args.warmup, world, rank, local, None, e2e_steps=0, keep_rule=2)
+        extra["full_depth_random_ablation"] = {
+            "workload": FULL.name, "keep_rule": 2, "kept": r3["k"], "us_per_step": r3["ms_max"] * 1e3,
+            "GB_per_s": r3["alg_bytes"] / (r3["ms_max"] * 1e-3) / 1e9, "scan_us": r3["scan_ms"] * 1e3,
+            "gather_us": r3["gather_ms"] * 1e3,
+            "note": "Random at the discrepancy rule's kept count (radix select of SplitMix64 priorities in the scan)"}
         from synth.workloads import HS_PREFIX, MID, ROLLOUT, TINY
         extra["tiny_fp32_single_prune"] = run_last_eviction(TINY, reps=20)
         extra["mid_bf16_single_eviction"] = run_last_eviction(MID, reps=20)

@@ -73,7 +73,9 @@ typedef struct dcp_cache {
 
 typedef struct dcp_config {
   float gamma;               /* threshold on l; the page's value is 0.10 [limits] */
-  int32_t keep_rule;         /* 0: keep l > gamma (DeCoPrune [how]); 1: the reverse criterion, keep !(l > gamma) */
+  int32_t keep_rule;         /* 0: keep l > gamma (DeCoPrune [how]); 1: the reverse criterion, keep !(l > gamma);
+                                2: the Random ablation [limits]: keep as many tokens as rule 0 would, drawn uniformly
+                                without replacement (see dcp_score_mask) */
   int32_t sink_chunks;       /* protected leading chunks [how] */
   int32_t window_chunks;     /* w: most recent chunks kept dense [how] */
   int32_t tokens_per_frame;  /* T latent tokens per latent frame */
@@ -87,7 +89,7 @@ typedef struct dcp_config {
   int32_t g_mode;
   int32_t rephase_sink;      /* must be 0: the sink keeps its stored phase */
   int32_t max_frames;        /* largest q0 (latent frame index) the workspace is sized for */
-  int32_t reserved;          /* must be 0 */
+  uint32_t random_seed;      /* keep_rule 2: a prune step draws from stream (random_seed << 32) | evict_first_frame */
 } dcp_config;
 
 /* Bytes of device workspace the cache/config need (prune, compact, re-index and score calls for this cache). */
@@ -103,14 +105,24 @@ dcp_status dcp_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream
  *   x0hat_dev, xref_dev : fp32 [n_tok][d] row-major (the probe-step clean prediction and the final output, or the
  *                         re-noised prediction and the clean observed chunk in the prefix pass).
  *   ell_dev   (nullable): fp32 [n_tok] out, l[n] = (1/d) sum_j (x0hat[n][j] - xref[n][j])^2, fp32 arithmetic.
+ *   keep_rule           : 0 keep l > gamma; 1 keep !(l > gamma); 2 the Random ablation of section "premises and
+ *                         limits" (Random at the same compression ratio): keep exactly as many tokens as rule 0, the
+ *                         ones with the smallest priorities z_n = n-th output (0-based) of a SplitMix64 sequence
+ *                         (Steele, Lea & Flood 2014) seeded with random_stream.  The priorities of one stream are
+ *                         distinct, so the kept set is unique.  Its cost grows with n_tok in one CTA (a radix
+ *                         select of up to 8 passes over the chunk's priorities).
+ *   random_stream       : SplitMix64 seed of rule 2 (ignored otherwise).  dcp_prune_step uses
+ *                         ((uint64_t)cfg->random_seed << 32) | (uint32_t)evict_first_frame.
  *   mask_dev  (nullable): uint8 [n_tok] out, 1 = keep (rule from keep_rule).
  *   idx_dev   (nullable): int32 [n_tok] out, increasing kept positions in [0, kept).
  *   kept_dev  (nullable): int32 out, number of kept tokens.
  *   status_dev          : int32 device status word (no device error is produced by this call today).
- * Errors: DCP_EINVAL for null inputs, n_tok < 1 or > 2^30, d < 1, non-finite gamma, short workspace. */
+ * Errors: DCP_EINVAL for null inputs, n_tok < 1 or > 2^30, d < 1, non-finite gamma, keep_rule outside {0, 1, 2},
+ * short workspace. */
 dcp_status dcp_score_mask(const float* x0hat_dev, const float* xref_dev, int32_t n_tok, int32_t d, float gamma,
-                          int32_t keep_rule, float* ell_dev, uint8_t* mask_dev, int32_t* idx_dev, int32_t* kept_dev,
-                          int32_t* status_dev, void* workspace_dev, size_t ws_bytes, void* stream);
+                          int32_t keep_rule, uint64_t random_stream, float* ell_dev, uint8_t* mask_dev,
+                          int32_t* idx_dev, int32_t* kept_dev, int32_t* status_dev, void* workspace_dev,
+                          size_t ws_bytes, void* stream);
 
 /* Physical compaction of the leaving chunk [how] with the fused key re-phase [differs].
  * The chunk in ring slot evict_slot (its first latent frame is evict_first_frame) is compacted: for every

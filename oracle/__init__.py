@@ -75,6 +75,9 @@ def lib():
             "oracle_rope_reindex": ([pc, pcfg, i32, i32], i32),
             "oracle_prune_step": ([pc, pcfg, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp], i32),
             "oracle_pr_chunk": ([vp, i64, i64, i64, i64, vp, vp], None),
+            "oracle_snapshot_size": ([pc, pcfg, ctypes.c_uint32], i64),
+            "oracle_snapshot": ([pc, pcfg, ctypes.c_uint32, i32, vp, i64], i32),
+            "oracle_restore": ([pc, pcfg, vp, i64, vp, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -241,3 +244,26 @@ def pr_chunk(hist_len: np.ndarray, sink_visible: int, window_visible: int, prior
     hl = np.ascontiguousarray(hist_len, np.int32)
     lib().oracle_pr_chunk(_p(hl), hl.shape[0], sink_visible, window_visible, prior, ctypes.byref(v), ctypes.byref(f))
     acc[0], acc[1] = v.value, f.value
+
+
+def snapshot(cache: HostCache, cfg: Cfg, live_slots: int, q0: int) -> np.ndarray:
+    """Host image of the cache's non-derivable state (sink, history rows, live ring slots, hist_len, hist_t, q0)."""
+    cc, oc = cache.c(), cfg.c()
+    n = lib().oracle_snapshot_size(ctypes.byref(cc), ctypes.byref(oc), live_slots)
+    if n < 0:
+        raise ValueError("snapshot refused")
+    out = np.empty(n, np.uint8)
+    rc = lib().oracle_snapshot(ctypes.byref(cc), ctypes.byref(oc), live_slots, q0, _p(out), n)
+    if rc != OK:
+        raise ValueError(f"snapshot refused: {rc}")
+    return out
+
+
+def restore(cache: HostCache, cfg: Cfg, image: np.ndarray):
+    """Restore an image into the cache in place; returns (rc, q0, live_slots)."""
+    cc, oc = cache.c(), cfg.c()
+    q0, live = ctypes.c_int32(0), ctypes.c_uint32(0)
+    img = np.ascontiguousarray(image, np.uint8)
+    rc = lib().oracle_restore(ctypes.byref(cc), ctypes.byref(oc), _p(img), img.shape[0], ctypes.byref(q0),
+                              ctypes.byref(live))
+    return rc, q0.value, live.value

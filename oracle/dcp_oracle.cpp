@@ -303,4 +303,155 @@ void oracle_pr_chunk(const int32_t* hist_len, int64_t n_planes, int64_t sink_tok
   *full += n_planes * prior_tokens;
 }
 
+// ------------------------------------------------------------------------------------------- host snapshot
+// Page "기술 요약: 생성형 월드 모델을 위한 지속적 계산 상태" (gist.science/ko/paper/2607.21686), section "PCS contract":
+// a checkpoint / restore pair whose restore gives back a state equal to the original (round trip) and whose
+// checkpoint holds exactly the state that cannot be re-derived (snapshot completeness).  For the pruned cache that
+// state is: every plane's sink rows and its history rows [0, hist_len), the live ring slots of the dense window,
+// hist_len, hist_t[0, longest history) and the query frame q0.  Rows past a plane's history and ring slots that
+// are not live are free space and are not saved.
+//
+// Image (little-endian), all offsets in bytes:
+//   [0, 128)    header: "DCPSNAP1", int32 L, H, D, dtype, int64 cap, hist_cap, sink_rows, chunk_rows,
+//               int32 window_chunks, uint32 live_slots (bit s = ring slot s is live), int32 q0, int32 hist_t_len,
+//               int64 row_bytes, rows_per_tensor, total_bytes, zero padding
+//   [128, ...)  int32 hist_len[L*H], then int32 hist_t[hist_t_len] (hist_t_len = longest history)
+//   data_off = first multiple of 256 after those: K block, then V block; each block holds, plane by plane, the
+//               plane's sink rows and history rows [0, hist_len[p]) (one run: they are adjacent in the cache),
+//               then its live ring slots in increasing slot order (chunk_rows rows each).
+static int64_t snap_align256(int64_t x) { return (x + 255) & ~(int64_t)255; }
+
+struct snap_geom {
+  int64_t C, sink_rows, row_bytes, n_planes, rows_per_tensor, hist_t_len, data_off, total;
+  int32_t n_live;
+};
+
+static int32_t snap_geometry(const oracle_cache* c, const oracle_config* cfg, uint32_t live_slots, snap_geom* g) {
+  g->C = (int64_t)cfg->tokens_per_frame * cfg->frames_per_chunk;
+  g->sink_rows = (int64_t)cfg->sink_chunks * g->C;
+  g->row_bytes = (int64_t)c->D * elem_size(c->dtype);
+  g->n_planes = (int64_t)c->L * c->H;
+  if (cfg->window_chunks + 1 > 32) return ORACLE_EINVAL;
+  if (cfg->window_chunks + 1 < 32 && (live_slots >> (cfg->window_chunks + 1)) != 0) return ORACLE_EINVAL;
+  g->n_live = 0;
+  for (int32_t s = 0; s <= cfg->window_chunks; ++s) g->n_live += (live_slots >> s) & 1u;
+  g->rows_per_tensor = 0;
+  g->hist_t_len = 0;
+  for (int64_t p = 0; p < g->n_planes; ++p) {
+    if (c->hist_len[p] < 0 || c->hist_len[p] > c->hist_cap) return ORACLE_EINVAL;
+    g->rows_per_tensor += g->sink_rows + c->hist_len[p] + (int64_t)g->n_live * g->C;
+    if (c->hist_len[p] > g->hist_t_len) g->hist_t_len = c->hist_len[p];
+  }
+  g->data_off = snap_align256(128 + 4 * g->n_planes + 4 * g->hist_t_len);
+  g->total = g->data_off + 2 * g->rows_per_tensor * g->row_bytes;
+  return ORACLE_OK;
+}
+
+int64_t oracle_snapshot_size(const oracle_cache* c, const oracle_config* cfg, uint32_t live_slots) {
+  snap_geom g;
+  return snap_geometry(c, cfg, live_slots, &g) == ORACLE_OK ? g.total : -1;
+}
+
+static void put_i32(uint8_t* b, int64_t off, int32_t x) { std::memcpy(b + off, &x, 4); }
+static void put_i64(uint8_t* b, int64_t off, int64_t x) { std::memcpy(b + off, &x, 8); }
+static int32_t get_i32(const uint8_t* b, int64_t off) { int32_t x; std::memcpy(&x, b + off, 4); return x; }
+static int64_t get_i64(const uint8_t* b, int64_t off) { int64_t x; std::memcpy(&x, b + off, 8); return x; }
+
+// The plane's saved rows in image order: (first cache row, row count) runs.
+static int32_t snap_runs(const oracle_cache* c, const oracle_config* cfg, const snap_geom& g, uint32_t live_slots,
+                         int64_t p, int64_t* first, int64_t* count) {
+  int32_t n = 0;
+  first[n] = 0;
+  count[n++] = g.sink_rows + c->hist_len[p];
+  for (int32_t s = 0; s <= cfg->window_chunks; ++s)
+    if ((live_slots >> s) & 1u) {
+      first[n] = g.sink_rows + c->hist_cap + (int64_t)s * g.C;
+      count[n++] = g.C;
+    }
+  return n;
+}
+
+int32_t oracle_snapshot(const oracle_cache* c, const oracle_config* cfg, uint32_t live_slots, int32_t q0,
+                        uint8_t* out, int64_t out_bytes) {
+  snap_geom g;
+  if (snap_geometry(c, cfg, live_slots, &g) != ORACLE_OK || out_bytes < g.total) return ORACLE_EINVAL;
+  std::memset(out, 0, (size_t)g.data_off);
+  std::memcpy(out, "DCPSNAP1", 8);
+  put_i32(out, 8, c->L);
+  put_i32(out, 12, c->H);
+  put_i32(out, 16, c->D);
+  put_i32(out, 20, c->dtype);
+  put_i64(out, 24, c->cap);
+  put_i64(out, 32, c->hist_cap);
+  put_i64(out, 40, g.sink_rows);
+  put_i64(out, 48, g.C);
+  put_i32(out, 56, cfg->window_chunks);
+  put_i32(out, 60, (int32_t)live_slots);
+  put_i32(out, 64, q0);
+  put_i32(out, 68, (int32_t)g.hist_t_len);
+  put_i64(out, 72, g.row_bytes);
+  put_i64(out, 80, g.rows_per_tensor);
+  put_i64(out, 88, g.total);
+  for (int64_t p = 0; p < g.n_planes; ++p) put_i32(out, 128 + 4 * p, c->hist_len[p]);
+  for (int64_t j = 0; j < g.hist_t_len; ++j) put_i32(out, 128 + 4 * g.n_planes + 4 * j, c->hist_t[j]);
+  int64_t first[33], count[33];
+  for (int32_t tensor = 0; tensor < 2; ++tensor) {
+    void* base = tensor == 0 ? c->k : c->v;
+    int64_t off = g.data_off + tensor * g.rows_per_tensor * g.row_bytes;
+    for (int64_t p = 0; p < g.n_planes; ++p) {
+      int32_t n = snap_runs(c, cfg, g, live_slots, p, first, count);
+      for (int32_t r = 0; r < n; ++r)
+        for (int64_t i = 0; i < count[r]; ++i) {
+          std::memcpy(out + off, row_ptr(base, c, p, first[r] + i), (size_t)g.row_bytes);
+          off += g.row_bytes;
+        }
+    }
+  }
+  return ORACLE_OK;
+}
+
+// Restore an image into a cache of the same geometry: the saved rows, hist_len and hist_t come back; free rows of
+// the cache are left as they are.
+int32_t oracle_restore(oracle_cache* c, const oracle_config* cfg, const uint8_t* in, int64_t in_bytes,
+                       int32_t* q0_out, uint32_t* live_out) {
+  if (in_bytes < 128 || std::memcmp(in, "DCPSNAP1", 8) != 0) return ORACLE_EINVAL;
+  const int64_t C = (int64_t)cfg->tokens_per_frame * cfg->frames_per_chunk;
+  if (get_i32(in, 8) != c->L || get_i32(in, 12) != c->H || get_i32(in, 16) != c->D || get_i32(in, 20) != c->dtype ||
+      get_i64(in, 24) != c->cap || get_i64(in, 32) != c->hist_cap || get_i64(in, 40) != cfg->sink_chunks * C ||
+      get_i64(in, 48) != C || get_i32(in, 56) != cfg->window_chunks)
+    return ORACLE_EINVAL;
+  const uint32_t live = (uint32_t)get_i32(in, 60);
+  const int64_t n_planes = (int64_t)c->L * c->H;
+  if (in_bytes < 128 + 4 * n_planes) return ORACLE_EINVAL;
+  std::vector<int32_t> saved_len((size_t)n_planes);
+  for (int64_t p = 0; p < n_planes; ++p) saved_len[(size_t)p] = get_i32(in, 128 + 4 * p);
+  // geometry of the image, from its own lengths
+  std::vector<int32_t> keep_len(c->hist_len, c->hist_len + n_planes);
+  for (int64_t p = 0; p < n_planes; ++p) c->hist_len[p] = saved_len[(size_t)p];
+  snap_geom g;
+  int32_t rc = snap_geometry(c, cfg, live, &g);
+  if (rc != ORACLE_OK || g.total != get_i64(in, 88) || g.total > in_bytes || g.hist_t_len != get_i32(in, 68) ||
+      g.rows_per_tensor != get_i64(in, 80) || g.row_bytes != get_i64(in, 72)) {
+    for (int64_t p = 0; p < n_planes; ++p) c->hist_len[p] = keep_len[(size_t)p];
+    return ORACLE_EINVAL;
+  }
+  for (int64_t j = 0; j < g.hist_t_len; ++j) c->hist_t[j] = get_i32(in, 128 + 4 * n_planes + 4 * j);
+  int64_t first[33], count[33];
+  for (int32_t tensor = 0; tensor < 2; ++tensor) {
+    void* base = tensor == 0 ? c->k : c->v;
+    int64_t off = g.data_off + tensor * g.rows_per_tensor * g.row_bytes;
+    for (int64_t p = 0; p < n_planes; ++p) {
+      int32_t n = snap_runs(c, cfg, g, live, p, first, count);
+      for (int32_t r = 0; r < n; ++r)
+        for (int64_t i = 0; i < count[r]; ++i) {
+          std::memcpy(row_ptr(base, c, p, first[r] + i), in + off, (size_t)g.row_bytes);
+          off += g.row_bytes;
+        }
+    }
+  }
+  if (q0_out) *q0_out = get_i32(in, 64);
+  if (live_out) *live_out = live;
+  return ORACLE_OK;
+}
+
 }  // extern "C"

@@ -92,7 +92,8 @@ def test_invalid_cache_rejected(bad):
     dict(tokens_per_frame=0), dict(frames_per_chunk=0), dict(window_chunks=-1), dict(sink_chunks=-1),
     dict(n_temporal_pairs=65), dict(n_temporal_pairs=-1), dict(pair_layout=1), dict(rephase_sink=1),
     dict(rope_base=0.0), dict(rope_base=float("nan")), dict(g_recent_R=11.0), dict(g_span_S=11.5),
-    dict(g_mode=2), dict(g_mode=1, g_span_S=-1.0), dict(keep_rule=2), dict(gamma=float("inf")), dict(max_frames=0)])
+    dict(g_mode=2), dict(g_mode=1, g_span_S=-1.0), dict(keep_rule=3), dict(keep_rule=-1),
+    dict(gamma=float("inf")), dict(max_frames=0)])
 def test_invalid_config_rejected(bad):
     assert _ws_size(_cache(), _cfg(**bad)) == 0
 
@@ -121,11 +122,11 @@ def test_invalid_other_entry_points_rejected():
     assert L.dcp_compact_layers(ctypes.byref(c), ctypes.byref(g), 9, 4, FAKE, None, 20, None, FAKE, n, None) == 1
     assert L.dcp_rope_reindex(ctypes.byref(c), ctypes.byref(g), 30, 20, FAKE, n, None) == 1
     assert L.dcp_rope_reindex(ctypes.byref(c), ctypes.byref(g), 20, 999, FAKE, n, None) == 1
-    assert L.dcp_score_mask(None, FAKE, 64, 16, 0.1, 0, None, None, None, None, FAKE, FAKE, 1 << 20, None) == 1
-    assert L.dcp_score_mask(FAKE, FAKE, 0, 16, 0.1, 0, None, None, None, None, FAKE, FAKE, 1 << 20, None) == 1
-    assert L.dcp_score_mask(FAKE, FAKE, 64, 16, 0.1, 3, None, None, None, None, FAKE, FAKE, 1 << 20, None) == 1
-    assert L.dcp_score_mask(FAKE, FAKE, 64, 16, 0.1, 0, None, None, None, None, None, FAKE, 1 << 20, None) == 1
-    assert L.dcp_score_mask(FAKE, FAKE, 64, 16, 0.1, 0, None, None, None, None, FAKE, FAKE, 8, None) == 1
+    assert L.dcp_score_mask(None, FAKE, 64, 16, 0.1, 0, 0, None, None, None, None, FAKE, FAKE, 1 << 20, None) == 1
+    assert L.dcp_score_mask(FAKE, FAKE, 0, 16, 0.1, 0, 0, None, None, None, None, FAKE, FAKE, 1 << 20, None) == 1
+    assert L.dcp_score_mask(FAKE, FAKE, 64, 16, 0.1, 3, 0, None, None, None, None, FAKE, FAKE, 1 << 20, None) == 1
+    assert L.dcp_score_mask(FAKE, FAKE, 64, 16, 0.1, 0, 0, None, None, None, None, None, FAKE, 1 << 20, None) == 1
+    assert L.dcp_score_mask(FAKE, FAKE, 64, 16, 0.1, 0, 0, None, None, None, None, FAKE, FAKE, 8, None) == 1
     assert L.dcp_workspace_init(None, 1024, None) == 1
     assert L.dcp_get_status(None, None) == 1
     assert L.dcp_reset_status(None, None) == 1

@@ -108,6 +108,21 @@ def test_reverse_criterion(gpu):
     gpu_vs_oracle_step(TINY_ROT, hc, ev, keep_rule=1)
 
 
+@pytest.mark.parametrize("seed", [0, 0x5EED1234])
+def test_random_ablation_step(gpu, seed):
+    """Random at the discrepancy rule's kept count (section 'premises and limits'): the same rows move, bit-exact, as
+    in the oracle drawing from the same SplitMix64 stream."""
+    hc, ev = replay.state_before_last(TINY_ROT)
+    o, g, idx, _ = gpu_vs_oracle_step(TINY_ROT, hc, ev, keep_rule=2, random_seed=seed)
+    assert 0 < len(idx) < TINY_ROT.C
+
+
+def test_random_ablation_mid(gpu):
+    """Random ablation on the mid bf16 eviction (6240 tokens: the radix select runs several passes)."""
+    hc, ev = replay.state_before_last(MID)
+    gpu_vs_oracle_step(MID, hc, ev, keep_rule=2, random_seed=77)
+
+
 def test_fp32_rows_not_power_of_two(gpu):
     """fp32 keys with D = 36 (144-byte rows, 9 vectors per row) take the general index path."""
     w = scaled(TINY_ROT, D=36, n_temporal_pairs=7, d=10)
@@ -123,14 +138,15 @@ def test_bf16_small_head_dim(gpu):
 
 # ------------------------------------------------------------------------------------------ standalone entry points
 @pytest.mark.parametrize("n_tok,d", [(1, 16), (64, 16), (6240, 64), (100003, 64), (777, 128), (500, 10), (300, 3)])
-@pytest.mark.parametrize("keep_rule", [0, 1])
+@pytest.mark.parametrize("keep_rule", [0, 1, 2])
 def test_score_mask(gpu, n_tok, d, keep_rule):
     x = synth.normal_f32(n_tok * d, 31, 1).reshape(n_tok, d)
     z = synth.normal_f32(n_tok * d, 31, 2).reshape(n_tok, d)
     s = 0.05 * np.exp(synth.uniform_f64(n_tok, 31, 3) * np.log(20.0))
     x0 = (x.astype(np.float64) + s[:, None] * z).astype(np.float32)
     ell = oracle.score(x0, x)
-    mask = oracle.keep(ell, 0.10, keep_rule)
+    stream = (0xD1CE << 32) | n_tok
+    mask = oracle.keep_random(ell, 0.10, stream) if keep_rule == 2 else oracle.keep(ell, 0.10, keep_rule)
     idx = oracle.indices(mask)
     band = np.abs(ell.astype(np.float64) - np.float32(0.10)) < 1e-6
     ws = dcp.new_workspace(dcp.dcp_score_workspace_size(n_tok))
@@ -140,7 +156,8 @@ def test_score_mask(gpu, n_tok, d, keep_rule):
     kept = torch.empty(1, dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for _ in range(2):  # the workspace must come back ready for the next call
-        dcp.dcp_score_mask(_cuda(x0), _cuda(x), 0.10, keep_rule, g_ell, g_mask, g_idx, kept, status, ws)
+        dcp.dcp_score_mask(_cuda(x0), _cuda(x), 0.10, keep_rule, g_ell, g_mask, g_idx, kept, status, ws,
+                           random_stream=stream)
         assert dcp.dcp_get_status(status) == dcp.DCP_OK
         if band.any():
             pytest.skip("seeded input lands in the tie band")
