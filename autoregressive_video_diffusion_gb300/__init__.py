@@ -77,6 +77,10 @@ _SIGS = {
     "dcp_abi_struct_sizes": ([], ctypes.c_uint32),
     "dcp_set_phase_events": ([_vp, _vp], _i32),
     "dcp_prune_step_noalloc": ([_pc, _pg, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
+    "dcp_snapshot_max_bytes": ([_pc, _pg, ctypes.c_uint32], _sz),
+    "dcp_snapshot": ([_pc, _pg, ctypes.c_uint32, _i32, _vp, _sz, _vp, _sz, _vp], _i32),
+    "dcp_restore": ([_pc, _pg, _vp, _sz, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_uint32), _vp, _sz, _vp],
+                    _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -273,3 +277,40 @@ def dcp_set_phase_events(ev_after_scan, ev_after_gather) -> None:
     a = None if ev_after_scan is None else ev_after_scan.cuda_event
     b = None if ev_after_gather is None else ev_after_gather.cuda_event
     _check(lib.dcp_set_phase_events(a, b), "dcp_set_phase_events")
+
+
+# ------------------------------------------------------------------------------------------ host snapshot
+def dcp_snapshot_max_bytes(cache: KVCache, cfg: Config, live_slots: int) -> int:
+    cc, gc = cache.c(), cfg.c()
+    n = lib.dcp_snapshot_max_bytes(ctypes.byref(cc), ctypes.byref(gc), live_slots)
+    if n == 0:
+        raise DcpError("dcp_snapshot_max_bytes", DCP_EINVAL)
+    return n
+
+
+def new_snapshot_image(nbytes: int) -> torch.Tensor:
+    """Page-locked, 256-byte aligned host buffer for a snapshot image (torch allocation; not on the hot path)."""
+    buf = torch.empty(nbytes + 256, dtype=torch.uint8, pin_memory=True)
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + nbytes]
+
+
+def snapshot_total_bytes(image: torch.Tensor) -> int:
+    """Size written by the snapshot held in `image` (its header's total_bytes; read after the stream synced)."""
+    return int(image[88:96].view(torch.int64).item())
+
+
+def dcp_snapshot(cache: KVCache, cfg: Config, live_slots: int, q0: int, image: torch.Tensor, ws: torch.Tensor,
+                 stream=None) -> None:
+    cc, gc = cache.c(), cfg.c()
+    _check(lib.dcp_snapshot(ctypes.byref(cc), ctypes.byref(gc), live_slots, q0, _ptr(image), image.numel(),
+                            _ptr(ws), ws.numel(), _stream(stream)), "dcp_snapshot")
+
+
+def dcp_restore(cache: KVCache, cfg: Config, image: torch.Tensor, ws: torch.Tensor, stream=None):
+    """Returns (q0, live_slots) of the image."""
+    cc, gc = cache.c(), cfg.c()
+    q0, live = ctypes.c_int32(0), ctypes.c_uint32(0)
+    _check(lib.dcp_restore(ctypes.byref(cc), ctypes.byref(gc), _ptr(image), image.numel(), ctypes.byref(q0),
+                           ctypes.byref(live), _ptr(ws), ws.numel(), _stream(stream)), "dcp_restore")
+    return q0.value, live.value

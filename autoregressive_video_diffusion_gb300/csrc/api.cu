@@ -184,6 +184,70 @@ RephaseParams rephase_params(const dcp_cache* c, const dcp_config* g, const Deri
 
 dcp_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? DCP_OK : DCP_ECUDA; }
 
+// ------------------------------------------------------------------------------------------ snapshot helpers
+dcp_status check_live(const dcp_config* g, uint32_t live_slots, int* n_live) {
+  if (g->window_chunks + 1 > 32) return DCP_EINVAL;
+  if (g->window_chunks + 1 < 32 && (live_slots >> (g->window_chunks + 1)) != 0) return DCP_EINVAL;
+  int n = 0;
+  for (int s = 0; s < 32; ++s) n += (live_slots >> s) & 1u;
+  *n_live = n;
+  return DCP_OK;
+}
+
+// Device address of a host image: page-locked host memory (cudaHostAlloc, cudaHostRegister) that the device reaches
+// through unified addressing.
+char* image_device_ptr(const void* img) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, img) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+  return static_cast<char*>(a.devicePointer);
+}
+
+int64_t img_i64(const void* img, int64_t off) {
+  int64_t x;
+  std::memcpy(&x, static_cast<const char*>(img) + off, 8);
+  return x;
+}
+
+int32_t img_i32(const void* img, int64_t off) {
+  int32_t x;
+  std::memcpy(&x, static_cast<const char*>(img) + off, 4);
+  return x;
+}
+
+SnapParams snap_params(const dcp_cache* c, const dcp_config* g, const Derived& d, uint32_t live_slots, int n_live,
+                       char* img_dev, size_t img_bytes, void* ws, int dir) {
+  SnapParams p{};
+  p.dir = dir;
+  p.k = static_cast<char*>(c->k);
+  p.v = static_cast<char*>(c->v);
+  p.row_bytes = c->D * d.esize;
+  p.plane_bytes = c->cap * (int64_t)p.row_bytes;
+  p.n_planes = (int32_t)d.n_planes;
+  p.sink_rows = d.sink_rows;
+  p.hist_cap = c->hist_cap;
+  p.C = d.C;
+  p.live_slots = live_slots;
+  p.n_live = n_live;
+  p.hist_len = c->hist_len;
+  p.hist_t = c->hist_t;
+  p.img = img_dev;
+  p.img_bytes = (int64_t)img_bytes;
+  p.L = c->L;
+  p.H = c->H;
+  p.D = c->D;
+  p.dtype = c->dtype;
+  p.cap = c->cap;
+  p.window_chunks = g->window_chunks;
+  p.ctrl = at<Ctrl>(ws, 0);
+  p.plane_off = at<int64_t>(ws, d.lay.plane_off);
+  p.status = c->status;
+  return p;
+}
+
 }  // namespace
 
 namespace dcp {
@@ -350,6 +414,69 @@ dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const f
   if (kept_host_pinned)
     rc = cuda_ok(cudaMemcpyAsync(kept_host_pinned, &at<Ctrl>(ws, 0)->k, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
   return rc;
+}
+
+size_t dcp_snapshot_max_bytes(const dcp_cache* cache, const dcp_config* cfg, uint32_t live_slots) {
+  Derived d;
+  int n_live = 0;
+  if (check_cache_cfg(cache, cfg, &d) != DCP_OK || check_live(cfg, live_slots, &n_live) != DCP_OK) return 0;
+  const int64_t rows = d.n_planes * (d.sink_rows + cache->hist_cap + (int64_t)n_live * d.C);
+  const int64_t data_off = (128 + 4 * d.n_planes + 4 * cache->hist_cap + 255) & ~(int64_t)255;
+  return (size_t)(data_off + 2 * rows * (int64_t)cache->D * d.esize);
+}
+
+dcp_status dcp_snapshot(const dcp_cache* cache, const dcp_config* cfg, uint32_t live_slots, int32_t q0,
+                        void* image_host, size_t image_bytes, void* ws, size_t ws_bytes, void* stream) {
+  Derived d;
+  int n_live = 0;
+  if (check_cache_cfg(cache, cfg, &d) != DCP_OK || check_live(cfg, live_slots, &n_live) != DCP_OK) return DCP_EINVAL;
+  if (check_ws(ws, ws_bytes, d.lay.total) != DCP_OK) return DCP_EINVAL;
+  if (!image_host || !aligned(image_host, 16) || image_bytes < 128) return DCP_EINVAL;
+  char* img = image_device_ptr(image_host);
+  if (!img || !aligned(img, 16)) return DCP_EINVAL;
+  SnapParams p = snap_params(cache, cfg, d, live_slots, n_live, img, image_bytes, ws, 0);
+  p.q0 = q0;
+  return cuda_ok(launch_snapshot(p, (cudaStream_t)stream));
+}
+
+dcp_status dcp_restore(const dcp_cache* cache, const dcp_config* cfg, const void* image_host, size_t image_bytes,
+                       int32_t* q0_out, uint32_t* live_slots_out, void* ws, size_t ws_bytes, void* stream) {
+  Derived d;
+  if (check_cache_cfg(cache, cfg, &d) != DCP_OK) return DCP_EINVAL;
+  if (check_ws(ws, ws_bytes, d.lay.total) != DCP_OK) return DCP_EINVAL;
+  if (!image_host || !aligned(image_host, 16) || image_bytes < 128) return DCP_EINVAL;
+  char* img = image_device_ptr(image_host);
+  if (!img || !aligned(img, 16)) return DCP_EINVAL;
+  // the image is complete in host memory: check it against this cache before anything is launched
+  const char* h = static_cast<const char*>(image_host);
+  const int64_t row_bytes = (int64_t)cache->D * d.esize;
+  if (std::memcmp(h, "DCPSNAP1", 8) != 0) return DCP_EINVAL;
+  if (img_i32(h, 8) != cache->L || img_i32(h, 12) != cache->H || img_i32(h, 16) != cache->D ||
+      img_i32(h, 20) != cache->dtype || img_i64(h, 24) != cache->cap || img_i64(h, 32) != cache->hist_cap ||
+      img_i64(h, 40) != d.sink_rows || img_i64(h, 48) != d.C || img_i32(h, 56) != cfg->window_chunks ||
+      img_i64(h, 72) != row_bytes)
+    return DCP_EINVAL;
+  const uint32_t live = (uint32_t)img_i32(h, 60);
+  int n_live = 0;
+  if (check_live(cfg, live, &n_live) != DCP_OK) return DCP_EINVAL;
+  if ((int64_t)image_bytes < 128 + 4 * d.n_planes) return DCP_EINVAL;
+  int64_t rows = 0;
+  int32_t longest = 0;
+  for (int64_t p = 0; p < d.n_planes; ++p) {
+    const int32_t len = img_i32(h, 128 + 4 * p);
+    if (len < 0 || len > cache->hist_cap) return DCP_EINVAL;
+    rows += d.sink_rows + len + (int64_t)n_live * d.C;
+    if (len > longest) longest = len;
+  }
+  const int64_t data_off = (128 + 4 * d.n_planes + 4 * (int64_t)longest + 255) & ~(int64_t)255;
+  const int64_t total = data_off + 2 * rows * row_bytes;
+  if (img_i32(h, 68) != longest || img_i64(h, 80) != rows || img_i64(h, 88) != total ||
+      (int64_t)image_bytes < total)
+    return DCP_EINVAL;
+  if (q0_out) *q0_out = img_i32(h, 64);
+  if (live_slots_out) *live_slots_out = live;
+  SnapParams p = snap_params(cache, cfg, d, live, n_live, img, image_bytes, ws, 1);
+  return cuda_ok(launch_snapshot(p, (cudaStream_t)stream));
 }
 
 dcp_status dcp_workspace_outputs(const dcp_cache* cache, const dcp_config* cfg, void* ws, float** ell_dev,

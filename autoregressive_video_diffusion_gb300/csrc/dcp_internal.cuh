@@ -17,8 +17,8 @@ constexpr int kMaxTile = 256;          // tokens per scan tile (one token per th
 // at zero (a zeroed workspace) and the final CTA puts them back to zero at the end of every call.
 struct Ctrl {
   uint32_t done;            // CTAs of the scan kernel that finished
-  int32_t reserved0;
-  int32_t reserved1;
+  int32_t snap_abort;       // snapshot / restore: nonzero -> the copy kernel does nothing
+  int32_t snap_hist_t_len;  // snapshot / restore: longest history of the image
   int32_t abort;            // verdict: nonzero -> the later kernels of the call do nothing
   int32_t k;                // kept tokens
   int32_t has_dyn;          // at least one plane receives the kept rows
@@ -31,18 +31,19 @@ struct Ctrl {
   int32_t acc_first_inv;    // max over receiving planes of INT32_MAX - plane
   int32_t acc_rp_max;       // max over all planes of hist_len
   int32_t acc_bad;          // some plane's hist_len is outside [0, hist_cap]
-  int32_t pad[50];
+  int64_t snap_rows;        // snapshot / restore: saved rows per tensor
+  int64_t snap_data_off;    // snapshot / restore: byte offset of the K block in the image
+  int32_t pad[46];
 };
 static_assert(sizeof(Ctrl) == 256, "ctrl block is one 256-byte line");
 
 struct Layout {           // byte offsets inside the workspace
-  size_t bits, ell, mask, idx, trig_g, rot_g, trig_h, rot_h, total;
+  size_t bits, ell, mask, idx, trig_g, rot_g, trig_h, rot_h, plane_off, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 inline Layout make_layout(int64_t n_tok, int64_t n_planes, int64_t F, int64_t n_t, int64_t max_frames) {
-  (void)n_planes;
   Layout L{};
   size_t off = sizeof(Ctrl);
   L.bits = off;       off = align256(off + 4 * (size_t)((n_tok + 31) / 32));
@@ -53,6 +54,7 @@ inline Layout make_layout(int64_t n_tok, int64_t n_planes, int64_t F, int64_t n_
   L.rot_g = off;      off = align256(off + (size_t)F);
   L.trig_h = off;     off = align256(off + 16 * (size_t)(max_frames * n_t));
   L.rot_h = off;      off = align256(off + (size_t)max_frames);
+  L.plane_off = off;  off = align256(off + 8 * (size_t)(n_planes > 0 ? n_planes + 1 : 0));
   L.total = off;
   return L;
 }
@@ -142,7 +144,31 @@ struct RephaseParams {
   int32_t* status;
 };
 
+// Snapshot / restore of the cache's non-derivable state to / from a host image (layout documented in dcp.h).
+struct SnapParams {
+  int32_t dir;             // 0: cache -> image (snapshot), 1: image -> cache (restore)
+  char* k;
+  char* v;
+  int64_t plane_bytes;
+  int32_t row_bytes;       // multiple of 16
+  int32_t n_planes;
+  int64_t sink_rows, hist_cap, C;
+  uint32_t live_slots;     // ring slots saved (bit s = slot s)
+  int32_t n_live;
+  int32_t* hist_len;       // cache, device
+  int32_t* hist_t;         // cache, device
+  char* img;               // device address of the host image (16-byte aligned)
+  int64_t img_bytes;
+  int32_t L, H, D, dtype;  // header fields of a snapshot
+  int64_t cap;
+  int32_t window_chunks, q0;
+  Ctrl* ctrl;
+  int64_t* plane_off;      // workspace [n_planes + 1]: first image row of each plane inside a tensor block
+  int32_t* status;
+};
+
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s);
+cudaError_t launch_snapshot(const SnapParams& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch);
 cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch);
 int sm_count();

@@ -341,11 +341,11 @@ class DeviceRollout:
         W.fill_device_history_canary(self.cache.k.data_ptr(), self.cache.v.data_ptr(), w, s)
         W.fill_device_chunks(self.cache.k.data_ptr(), self.cache.v.data_ptr(), w, list(range(w.sink_chunks)), s)
         self.placed = set(range(w.sink_chunks))
-        self.cfg = dcp.Config(gamma=w.gamma, keep_rule=keep_rule, sink_chunks=w.sink_chunks,
+        self.cfg = dcp.Config(gamma=w.gamma, keep_rule=0, sink_chunks=w.sink_chunks,
                               window_chunks=w.window_chunks, tokens_per_frame=w.tokens_per_frame,
                               frames_per_chunk=w.frames_per_chunk, n_temporal_pairs=w.n_temporal_pairs,
                               rope_base=w.rope_base, g_recent_R=w.R, g_span_S=w.S, g_mode=w.g_mode,
-                              max_frames=w.max_frames, random_seed=random_seed)
+                              max_frames=w.max_frames)
         self.ws = dcp.new_workspace(dcp.dcp_workspace_size(self.cache, self.cfg))
         self.static = head_is_static
         self.hs = None if head_is_static is None else torch.from_numpy(head_is_static).cuda()
@@ -493,6 +493,69 @@ def run_rollout(w):
     return out
 
 
+def run_snapshot(w, reps: int):
+    """Host snapshot and restore (dcp_snapshot / dcp_restore) of the state left by the full-depth eviction, cut to
+    w.L layers: sink, 947 history rows and the three live window chunks of every plane.  Compared with a plain copy
+    of the same byte count between the same page-locked buffer and the device (the link's own rate)."""
+    import torch
+
+    import autoregressive_video_diffusion_gb300 as dcp
+    from synth import workloads as W
+    c, q0_prev, q0 = w.evictions()[-1]
+    stream = torch.cuda.current_stream()
+    cache = dcp.KVCache(w.L, w.H, w.D, w.dtype, w.cap, w.hist_cap)
+    W.fill_device_chunks(cache.k.data_ptr(), cache.v.data_ptr(), w,
+                         list(range(w.sink_chunks)) + w.resident_window(c), stream.cuda_stream)
+    W.fill_device_history_canary(cache.k.data_ptr(), cache.v.data_ptr(), w, stream.cuda_stream)
+    cfg = dcp.Config(gamma=w.gamma, sink_chunks=w.sink_chunks, window_chunks=w.window_chunks,
+                     tokens_per_frame=w.tokens_per_frame, frames_per_chunk=w.frames_per_chunk,
+                     n_temporal_pairs=w.n_temporal_pairs, rope_base=w.rope_base, g_recent_R=w.R, g_span_S=w.S,
+                     g_mode=w.g_mode, max_frames=w.max_frames)
+    ws = dcp.new_workspace(dcp.dcp_workspace_size(cache, cfg))
+    x0, xr = (torch.from_numpy(x).cuda() for x in w.score_inputs(c))
+    dcp.dcp_prune_step(cache, cfg, x0, xr, w.slot_of(c), w.first_frame(c), q0_prev, q0, None, None, None, ws)
+    live = 0
+    for cc in range(c + 1, c + w.window_chunks + 1):
+        live |= 1 << w.slot_of(cc)
+    img = dcp.new_snapshot_image(dcp.dcp_snapshot_max_bytes(cache, cfg, live))
+    dcp.dcp_snapshot(cache, cfg, live, q0, img, ws)
+    torch.cuda.synchronize()
+    if dcp.dcp_get_status(cache.status) != dcp.DCP_OK:
+        raise RuntimeError("snapshot reported an error")
+    n = dcp.snapshot_total_bytes(img)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(fn):
+        out = []
+        for _ in range(reps):
+            ev[0].record(stream)
+            fn()
+            ev[1].record(stream)
+            ev[1].synchronize()
+            out.append(ev[0].elapsed_time(ev[1]))
+        return float(np.median(out))
+
+    snap_ms = timed(lambda: dcp.dcp_snapshot(cache, cfg, live, q0, img, ws))
+    rest_ms = timed(lambda: dcp.dcp_restore(cache, cfg, img, ws))
+    if dcp.dcp_get_status(cache.status) != dcp.DCP_OK:
+        raise RuntimeError("restore reported an error")
+    dev_buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+    host = img[:n]
+    d2h_ms = timed(lambda: host.copy_(dev_buf, non_blocking=True))
+    h2d_ms = timed(lambda: dev_buf.copy_(host, non_blocking=True))
+    gbs = lambda ms: n / (ms * 1e-3) / 1e9  # noqa: E731
+    out = {"workload": f"{w.name} cut to {w.L} layers, after its eviction", "image_bytes": n,
+           "history_rows_per_plane": int(cache.hist_len[0].item()), "live_window_chunks": w.window_chunks,
+           "snapshot_us": snap_ms * 1e3, "snapshot_GB_per_s": gbs(snap_ms),
+           "restore_us": rest_ms * 1e3, "restore_GB_per_s": gbs(rest_ms),
+           "plain_copy_d2h_GB_per_s": gbs(d2h_ms), "plain_copy_h2d_GB_per_s": gbs(h2d_ms),
+           "frac_of_plain_copy": {"snapshot": d2h_ms / snap_ms, "restore": h2d_ms / rest_ms},
+           "gpu_launches_per_call": 2}
+    del cache, dev_buf, img, host, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_entry_case(case: str, steps: int, warmup: int):
     """Single entry points on their own (one GPU), for per-kernel measurement and profiling captures:
     reindex: dcp_rope_reindex of a bf16 cache of 64 planes x 90,000 history rows (frames 4-219, ~417 rows per frame,
@@ -614,12 +677,20 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: the same workload with fewer layers (a few GB on the device)")
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before the timed region")
-    ap.add_argument("--case", default="step", choices=["step", "reindex", "score"],
+    ap.add_argument("--case", default="step", choices=["step", "reindex", "score", "snapshot"],
                     help="step: the prune step (default); reindex: dcp_rope_reindex of a 64-plane cache with 90,000 "
-                         "history rows per plane; score: dcp_score_mask of one full-depth chunk")
+                         "history rows per plane; score: dcp_score_mask of one full-depth chunk; snapshot: "
+                         "dcp_snapshot / dcp_restore of the state after the full-depth eviction cut to --layers "
+                         "(default 8) layers")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.case == "snapshot":
+        import __graft_entry__
+        __graft_entry__.build()
+        from synth.workloads import FULL, scaled
+        print(json.dumps({"case": "snapshot", **run_snapshot(scaled(FULL, L=args.layers or 8), reps=args.steps)}))
+        return
     if args.case != "step":
         run_entry_case(args.case, args.steps, args.warmup)
         return
@@ -685,6 +756,8 @@ def main():
         extra["mid_bf16_single_eviction"] = run_last_eviction(MID, reps=20)
         extra["head_specialised_prefix"] = run_head_specialised(HS_PREFIX, reps=3)
         extra["minute_rollout_gqa8"] = run_rollout(ROLLOUT)
+        from synth.workloads import scaled
+        extra["host_snapshot_restore"] = run_snapshot(scaled(FULL, L=8), reps=5)
     if rank != 0:
         return
     peak, peak_kind = _peaks()

@@ -177,6 +177,51 @@ dcp_status dcp_prune_step_noalloc(const dcp_cache* cache, const dcp_config* cfg,
                                   int32_t q0_prev, int32_t q0, const uint8_t* head_is_static_dev, int32_t* kept_dev,
                                   int32_t* kept_host_pinned, void* stream);
 
+/* ---------------------------------------------------------------------------------------------------------------
+ * Host snapshot and restore of the pruned cache.
+ * Page "기술 요약: 생성형 월드 모델을 위한 지속적 계산 상태" (gist.science/ko/paper/2607.21686), section "PCS contract":
+ * a checkpoint / restore pair where restore gives back the state (round trip) and the checkpoint holds exactly the
+ * state that cannot be re-derived (snapshot completeness).  For this cache that state is each plane's sink rows and
+ * history rows [0, hist_len), the live ring slots of the dense window (bit s of live_slots = ring slot s holds a
+ * chunk; window_chunks + 1 <= 32), hist_len, hist_t[0, longest history) and the query frame q0.  Rows past a
+ * plane's history and ring slots that are not live are free space: never saved, never written back.
+ *
+ * Image layout (little-endian, byte offsets):
+ *   [0, 128)   header: char magic[8] = "DCPSNAP1"; int32 L, H, D, dtype; int64 cap, hist_cap, sink_rows,
+ *              chunk_rows (C); int32 window_chunks; uint32 live_slots; int32 q0; int32 hist_t_len (longest
+ *              history); int64 row_bytes, rows_per_tensor, total_bytes; zero up to byte 128.
+ *   [128, ..)  int32 hist_len[L*H], then int32 hist_t[hist_t_len].
+ *   data_off   the first multiple of 256 at or after the end of hist_t (bytes in between are zero).  The K block
+ *              then the V block (rows_per_tensor rows each): plane by plane (plane = l*H + h), the plane's sink and
+ *              history rows [0, sink_rows + hist_len), then its live ring slots in increasing slot order (C rows
+ *              each).  total_bytes = data_off + 2 * rows_per_tensor * row_bytes.
+ * Images move between the device and page-locked host memory (cudaHostAlloc / cudaHostRegister, 16-byte aligned)
+ * by a kernel pair on the caller's stream (the device reaches the host image through unified addressing).
+ * --------------------------------------------------------------------------------------------------------------- */
+
+/* Image size when every plane's history is full: an upper bound for dcp_snapshot.  0 for an invalid
+ * cache/config or live_slots. */
+size_t dcp_snapshot_max_bytes(const dcp_cache* cache, const dcp_config* cfg, uint32_t live_slots);
+
+/* Write the cache's state into image_host (image_bytes long), stream-ordered, without host synchronisation: the
+ * image is complete once `stream` has reached this point.  Its total_bytes field (offset 88) gives the size used.
+ * Device errors: DCP_ECAPACITY (the image is too small: only the header is written, with the size needed),
+ * DCP_EDEVICE (a hist_len outside [0, hist_cap]: nothing but the header is written).
+ * Host errors: DCP_EINVAL (bad cache/config, live_slots with bits past the ring, image not page-locked host memory
+ * or not 16-byte aligned, image_bytes < 128, short workspace). */
+dcp_status dcp_snapshot(const dcp_cache* cache, const dcp_config* cfg, uint32_t live_slots, int32_t q0,
+                        void* image_host, size_t image_bytes, void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* Restore an image into a cache of the same geometry (L, H, D, dtype, cap, hist_cap, sink rows, C, window_chunks).
+ * The image must be complete when the call is made (any snapshot that wrote it has been synchronised): the host
+ * checks its header and lengths, fills q0_out / live_slots_out (nullable), then the copy is stream-ordered.  The
+ * saved rows, hist_len and hist_t come back; free rows of the cache are not touched.
+ * Host errors: DCP_EINVAL (bad magic, geometry that differs from the cache, inconsistent lengths or sizes,
+ * image_bytes short of total_bytes, image not page-locked, short workspace).  Nothing is launched then. */
+dcp_status dcp_restore(const dcp_cache* cache, const dcp_config* cfg, const void* image_host, size_t image_bytes,
+                       int32_t* q0_out, uint32_t* live_slots_out, void* workspace_dev, size_t ws_bytes,
+                       void* stream);
+
 /* Device addresses inside a prune-step workspace: l (fp32 [C]), the mask (uint8 [C]) and the index list
  * (int32 [C], first `kept` entries valid) of the last dcp_prune_step / dcp_compact_layers call. */
 dcp_status dcp_workspace_outputs(const dcp_cache* cache, const dcp_config* cfg, void* workspace_dev, float** ell_dev,
