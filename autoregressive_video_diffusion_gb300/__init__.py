@@ -53,6 +53,14 @@ class DcpConfigC(ctypes.Structure):
                 ("max_frames", ctypes.c_int32), ("random_seed", ctypes.c_uint32)]
 
 
+class DcpPagedCacheC(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("L", ctypes.c_int32),
+                ("H", ctypes.c_int32), ("D", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("layout", ctypes.c_int32), ("n_blocks", ctypes.c_int64),
+                ("hist_cap", ctypes.c_int64), ("hist_blocks", ctypes.c_void_p), ("window_blocks", ctypes.c_void_p),
+                ("hist_len", ctypes.c_void_p), ("hist_t", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+
+
 class DcpPrCounter(ctypes.Structure):
     _fields_ = [("visible", ctypes.c_int64), ("full", ctypes.c_int64)]
 
@@ -77,6 +85,10 @@ _SIGS = {
     "dcp_abi_struct_sizes": ([], ctypes.c_uint32),
     "dcp_set_phase_events": ([_vp, _vp], _i32),
     "dcp_prune_step_noalloc": ([_pc, _pg, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
+    "dcp_paged_workspace_size": ([ctypes.POINTER(DcpPagedCacheC), _pg], _sz),
+    "dcp_paged_prune_step": ([ctypes.POINTER(DcpPagedCacheC), _pg, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
+                              _vp, _vp, _sz, _vp], _i32),
+    "dcp_abi_paged_cache_size": ([], ctypes.c_uint32),
     "dcp_snapshot_max_bytes": ([_pc, _pg, ctypes.c_uint32], _sz),
     "dcp_snapshot": ([_pc, _pg, ctypes.c_uint32, _i32, _vp, _sz, _vp, _sz, _vp], _i32),
     "dcp_restore": ([_pc, _pg, _vp, _sz, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_uint32), _vp, _sz, _vp],
@@ -88,7 +100,8 @@ for _name, (_args, _res) in _SIGS.items():
     _fn.restype = _res
 
 _sizes = lib.dcp_abi_struct_sizes()
-if (_sizes >> 16) != ctypes.sizeof(DcpCacheC) or (_sizes & 0xFFFF) != ctypes.sizeof(DcpConfigC):
+if (_sizes >> 16) != ctypes.sizeof(DcpCacheC) or (_sizes & 0xFFFF) != ctypes.sizeof(DcpConfigC) or \
+        lib.dcp_abi_paged_cache_size() != ctypes.sizeof(DcpPagedCacheC):
     raise ImportError("libdcp struct layout does not match the binding")
 
 
@@ -314,3 +327,84 @@ def dcp_restore(cache: KVCache, cfg: Config, image: torch.Tensor, ws: torch.Tens
     _check(lib.dcp_restore(ctypes.byref(cc), ctypes.byref(gc), _ptr(image), image.numel(), ctypes.byref(q0),
                            ctypes.byref(live), _ptr(ws), ws.numel(), _stream(stream)), "dcp_restore")
     return q0.value, live.value
+
+
+# ------------------------------------------------------------------------------------------ paged variant
+DCP_PAGED_HND, DCP_PAGED_NHD = 0, 1
+
+
+class PagedKVCache:
+    """Device block pools and block tables of one paged KV cache (dcp_paged_cache).
+
+    Pools are [L][n_blocks][H][block_size][D] (HND) or [L][n_blocks][block_size][H][D] (NHD); hist_blocks and
+    window_blocks are int32 device tensors the caller fills (block ids of the history positions and of the ring
+    slots, slot s owning entries [s * C / block_size, (s + 1) * C / block_size))."""
+
+    def __init__(self, L: int, H: int, D: int, dtype: int, block_size: int, layout: int, n_blocks: int,
+                 hist_cap: int, n_window_blocks: int, device="cuda"):
+        tdt = torch.bfloat16 if dtype == DCP_BF16 else torch.float32
+        shape = (L, n_blocks, H, block_size, D) if layout == DCP_PAGED_HND else (L, n_blocks, block_size, H, D)
+        self.L, self.H, self.D, self.dtype = L, H, D, dtype
+        self.block_size, self.layout, self.n_blocks, self.hist_cap = block_size, layout, n_blocks, hist_cap
+        self.k_pool = torch.empty(shape, dtype=tdt, device=device)
+        self.v_pool = torch.empty(shape, dtype=tdt, device=device)
+        self.hist_blocks = torch.zeros(max(hist_cap // block_size, 1), dtype=torch.int32, device=device)
+        self.window_blocks = torch.zeros(max(n_window_blocks, 1), dtype=torch.int32, device=device)
+        self.hist_len = torch.zeros(L * H, dtype=torch.int32, device=device)
+        self.hist_t = torch.zeros(max(hist_cap, 1), dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def c(self) -> DcpPagedCacheC:
+        return DcpPagedCacheC(_ptr(self.k_pool), _ptr(self.v_pool), self.L, self.H, self.D, self.dtype,
+                              self.block_size, self.layout, self.n_blocks, self.hist_cap, _ptr(self.hist_blocks),
+                              _ptr(self.window_blocks), _ptr(self.hist_len), _ptr(self.hist_t), _ptr(self.status))
+
+
+def dcp_paged_workspace_size(cache: PagedKVCache, cfg: Config) -> int:
+    cc, gc = cache.c(), cfg.c()
+    n = lib.dcp_paged_workspace_size(ctypes.byref(cc), ctypes.byref(gc))
+    if n == 0:
+        raise DcpError("dcp_paged_workspace_size", DCP_EINVAL)
+    return n
+
+
+def dcp_paged_prune_step(cache: PagedKVCache, cfg: Config, x0hat: torch.Tensor, xref: torch.Tensor, evict_slot: int,
+                         evict_first_frame: int, q0_prev: int, q0: int, head_is_static, kept, kept_host,
+                         ws: torch.Tensor, stream=None) -> None:
+    cc, gc = cache.c(), cfg.c()
+    _check(lib.dcp_paged_prune_step(ctypes.byref(cc), ctypes.byref(gc), _ptr(x0hat), _ptr(xref), x0hat.shape[1],
+                                    evict_slot, evict_first_frame, q0_prev, q0, _ptr(head_is_static), _ptr(kept),
+                                    _ptr(kept_host), _ptr(ws), ws.numel(), _stream(stream)), "dcp_paged_prune_step")
+
+
+def paged_row_map(cfg: Config, hist_cap: int, block_size: int, sink_blocks: torch.Tensor, hist_blocks: torch.Tensor,
+                  window_blocks: torch.Tensor):
+    """(block, row-in-block) of every row of the contiguous layout sink | history | ring, as int64 tensors on the
+    tables' device.  For moving caches between the two layouts (set-up and checks; not on the prune path)."""
+    C = cfg.C
+    sink = cfg.sink_chunks * C
+    dev = hist_blocks.device
+    pos = torch.arange(sink + hist_cap + (cfg.window_chunks + 1) * C, device=dev)
+    block = torch.empty_like(pos)
+    region = [(0, sink, sink_blocks), (sink, sink + hist_cap, hist_blocks),
+              (sink + hist_cap, pos.numel(), window_blocks)]
+    for lo, hi, tbl in region:
+        i = pos[lo:hi] - lo
+        if hi > lo:
+            block[lo:hi] = tbl.to(device=dev, dtype=torch.int64)[i // block_size]
+    return block, pos % block_size
+
+
+def paged_pack(pool: torch.Tensor, t: torch.Tensor, block: torch.Tensor, off: torch.Tensor, layout: int) -> None:
+    """Write a contiguous [L][H][rows][D] tensor into a block pool through a row map."""
+    if layout == DCP_PAGED_HND:
+        pool[:, block, :, off, :] = t.permute(2, 0, 1, 3)
+    else:
+        pool[:, block, off] = t.permute(0, 2, 1, 3)
+
+
+def paged_unpack(pool: torch.Tensor, block: torch.Tensor, off: torch.Tensor, layout: int) -> torch.Tensor:
+    """Read a block pool back into a contiguous [L][H][rows][D] tensor through a row map."""
+    if layout == DCP_PAGED_HND:
+        return pool[:, block, :, off, :].permute(1, 2, 0, 3).contiguous()
+    return pool[:, block, off].permute(0, 2, 1, 3).contiguous()

@@ -218,6 +218,64 @@ int32_t img_i32(const void* img, int64_t off) {
   return x;
 }
 
+// ------------------------------------------------------------------------------------------ paged caches
+struct PagedView {
+  Paging pg;
+  const int32_t* window_blocks;
+  int64_t n_blocks;
+};
+
+// A paged cache seen as a dcp_cache (for the shared checks and parameters) plus its addressing.  The shadow's cap
+// is the row count of the contiguous layout with the same regions; the kernels never use it for a paged cache.
+dcp_status paged_view(const dcp_paged_cache* c, const dcp_config* g, dcp_cache* shadow, PagedView* pv) {
+  if (!c || !g) return DCP_EINVAL;
+  if (!c->hist_blocks || !c->window_blocks || !aligned(c->hist_blocks, 4) || !aligned(c->window_blocks, 4))
+    return DCP_EINVAL;
+  if (c->block_size < 1 || c->n_blocks < 1 || c->n_blocks > INT32_MAX) return DCP_EINVAL;
+  if (c->layout != DCP_PAGED_HND && c->layout != DCP_PAGED_NHD) return DCP_EINVAL;
+  if (g->tokens_per_frame < 1 || g->frames_per_chunk < 1 || g->window_chunks < 0 || g->sink_chunks < 0)
+    return DCP_EINVAL;
+  const int64_t C = (int64_t)g->tokens_per_frame * g->frames_per_chunk;
+  if (C % c->block_size || c->hist_cap < 0 || c->hist_cap % c->block_size) return DCP_EINVAL;
+  std::memset(shadow, 0, sizeof(*shadow));
+  shadow->k = c->k_pool;
+  shadow->v = c->v_pool;
+  shadow->L = c->L;
+  shadow->H = c->H;
+  shadow->D = c->D;
+  shadow->dtype = c->dtype;
+  shadow->hist_cap = c->hist_cap;
+  shadow->cap = (int64_t)g->sink_chunks * C + c->hist_cap + ((int64_t)g->window_chunks + 1) * C;
+  shadow->hist_len = c->hist_len;
+  shadow->hist_t = c->hist_t;
+  shadow->status = c->status;
+  if (c->H < 1 || c->D < 2) return DCP_EINVAL;
+  const int64_t rb = (int64_t)c->D * (c->dtype == DCP_BF16 ? 2 : 4);
+  const int64_t bs = c->block_size, H = c->H;
+  Paging pg{};
+  pg.H = c->H;
+  pg.bs = c->block_size;
+  if (c->layout == DCP_PAGED_HND) {
+    pg.s_row = rb;
+    pg.s_head = bs * rb;
+  } else {
+    pg.s_row = H * rb;
+    pg.s_head = rb;
+  }
+  pg.s_block = H * bs * rb;
+  pg.s_layer = c->n_blocks * pg.s_block;
+  pg.hist_blocks = c->hist_blocks;
+  pv->pg = pg;
+  pv->window_blocks = c->window_blocks;
+  pv->n_blocks = c->n_blocks;
+  return DCP_OK;
+}
+
+dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dcp_config* cfg, const float* x0hat,
+                           const float* xref, int32_t dd, int32_t evict_slot, int32_t evict_first_frame,
+                           int32_t q0_prev, int32_t q0, const uint8_t* head_is_static, int32_t* kept_dev,
+                           int32_t* kept_host_pinned, void* ws, size_t ws_bytes, void* stream);
+
 SnapParams snap_params(const dcp_cache* c, const dcp_config* g, const Derived& d, uint32_t live_slots, int n_live,
                        char* img_dev, size_t img_bytes, void* ws, int dir) {
   SnapParams p{};
@@ -341,7 +399,7 @@ dcp_status dcp_compact_layers(const dcp_cache* cache, const dcp_config* cfg, int
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
   return cuda_ok(
-      launch_gather(gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame), st, true));
+      launch_gather(gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame), st, true, false));
 }
 
 dcp_status dcp_rope_reindex(const dcp_cache* cache, const dcp_config* cfg, int32_t q0_prev, int32_t q0, void* ws,
@@ -361,13 +419,45 @@ dcp_status dcp_rope_reindex(const dcp_cache* cache, const dcp_config* cfg, int32
   finish_tables(sp);
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
-  return cuda_ok(launch_rephase(rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi), st, true));
+  return cuda_ok(launch_rephase(rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi), st, true, false));
 }
 
 dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const float* x0hat, const float* xref,
                           int32_t dd, int32_t evict_slot, int32_t evict_first_frame, int32_t q0_prev, int32_t q0,
                           const uint8_t* head_is_static, int32_t* kept_dev, int32_t* kept_host_pinned, void* ws,
                           size_t ws_bytes, void* stream) {
+  return prune_step_impl(cache, nullptr, cfg, x0hat, xref, dd, evict_slot, evict_first_frame, q0_prev, q0,
+                         head_is_static, kept_dev, kept_host_pinned, ws, ws_bytes, stream);
+}
+
+size_t dcp_paged_workspace_size(const dcp_paged_cache* cache, const dcp_config* cfg) {
+  dcp_cache shadow;
+  PagedView pv;
+  if (paged_view(cache, cfg, &shadow, &pv) != DCP_OK) return 0;
+  return dcp_workspace_size(&shadow, cfg);
+}
+
+dcp_status dcp_paged_prune_step(const dcp_paged_cache* cache, const dcp_config* cfg, const float* x0hat,
+                                const float* xref, int32_t dd, int32_t evict_slot, int32_t evict_first_frame,
+                                int32_t q0_prev, int32_t q0, const uint8_t* head_is_static, int32_t* kept_dev,
+                                int32_t* kept_host_pinned, void* ws, size_t ws_bytes, void* stream) {
+  dcp_cache shadow;
+  PagedView pv;
+  if (paged_view(cache, cfg, &shadow, &pv) != DCP_OK) return DCP_EINVAL;
+  return prune_step_impl(&shadow, &pv, cfg, x0hat, xref, dd, evict_slot, evict_first_frame, q0_prev, q0,
+                         head_is_static, kept_dev, kept_host_pinned, ws, ws_bytes, stream);
+}
+
+uint32_t dcp_abi_paged_cache_size(void) { return (uint32_t)sizeof(dcp_paged_cache); }
+
+}  // extern "C"
+
+namespace {
+
+dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dcp_config* cfg, const float* x0hat,
+                           const float* xref, int32_t dd, int32_t evict_slot, int32_t evict_first_frame,
+                           int32_t q0_prev, int32_t q0, const uint8_t* head_is_static, int32_t* kept_dev,
+                           int32_t* kept_host_pinned, void* ws, size_t ws_bytes, void* stream) {
   Derived d;
   if (check_cache_cfg(cache, cfg, &d) != DCP_OK) return DCP_EINVAL;
   if (check_eviction(cfg, d, evict_slot, evict_first_frame, q0) != DCP_OK) return DCP_EINVAL;
@@ -399,22 +489,40 @@ dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const f
   sp.q0 = q0;
   sp.q0_prev = q0_prev;
   finish_tables(sp);
+  GatherParams gp = gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame);
+  RephaseParams rp = rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi);
+  if (pv) {
+    const int64_t per_chunk = d.C / pv->pg.bs;
+    Paging pg = pv->pg;
+    pg.src_blocks = pv->window_blocks + (int64_t)evict_slot * per_chunk;
+    gp.pg = pg;
+    rp.pg = pg;
+    sp.tbl_a = pg.hist_blocks;
+    sp.n_tbl_a = (int32_t)(cache->hist_cap / pg.bs);
+    sp.tbl_b = pg.src_blocks;
+    sp.n_tbl_b = (int32_t)per_chunk;
+    sp.n_blocks = pv->n_blocks;
+    sp.n_tbl_slices = (sp.n_tbl_a + sp.n_tbl_b + kThreads - 1) / kThreads;
+  }
   // scan -> re-index (reads the history lengths before the step) -> gather (grows them)
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
   if (rephase) {
-    rc = cuda_ok(launch_rephase(rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi), st, true));
+    rc = cuda_ok(launch_rephase(rp, st, true, pv != nullptr));
     if (rc != DCP_OK) return rc;
   }
   if (g_ev_after_scan && cudaEventRecord(g_ev_after_scan, st) != cudaSuccess) return DCP_ECUDA;
-  rc = cuda_ok(launch_gather(gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame), st,
-                             g_ev_after_scan == nullptr));
+  rc = cuda_ok(launch_gather(gp, st, g_ev_after_scan == nullptr, pv != nullptr));
   if (rc != DCP_OK) return rc;
   if (g_ev_after_gather && cudaEventRecord(g_ev_after_gather, st) != cudaSuccess) return DCP_ECUDA;
   if (kept_host_pinned)
     rc = cuda_ok(cudaMemcpyAsync(kept_host_pinned, &at<Ctrl>(ws, 0)->k, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
   return rc;
 }
+
+}  // namespace
+
+extern "C" {
 
 size_t dcp_snapshot_max_bytes(const dcp_cache* cache, const dcp_config* cfg, uint32_t live_slots) {
   Derived d;

@@ -85,6 +85,12 @@ struct ScanParams {
   const uint8_t* head_is_static;
   int32_t n_planes, n_plane_slices;
   int64_t hist_cap;
+  // paged caches: every block-table entry the step will use must name a block of the pools (CTAs numbered below
+  // n_tbl_slices each check 256 entries of tbl_a followed by tbl_b)
+  const int32_t* tbl_a;
+  const int32_t* tbl_b;
+  int32_t n_tbl_a, n_tbl_b, n_tbl_slices;
+  int64_t n_blocks;
   // phase tables, built by the CTAs numbered past the tiles (kTableEntries entries each)
   int32_t n_trig_blocks;
   float4* trig_g;          // [F][n_t]: turn from t to t~(t; q0) for the leaving chunk's frames
@@ -106,6 +112,15 @@ constexpr int kTableEntries = 64;  // table entries per table CTA (fp64 work spr
 // when rows and base addresses are 32-byte aligned.
 constexpr int kBytesPerThread = 64;
 
+// Addressing of a paged cache (unused for the contiguous layout): plane (l, h) starts at l * s_layer + h * s_head;
+// position i of a region whose block table is tbl sits at tbl[i / bs] * s_block + (i % bs) * s_row from there.
+struct Paging {
+  int32_t H, bs;
+  int64_t s_layer, s_head, s_block, s_row;
+  const int32_t* src_blocks;   // gather: the leaving ring slot's blocks
+  const int32_t* hist_blocks;  // history blocks
+};
+
 struct GatherParams {
   char* k;
   char* v;
@@ -124,6 +139,7 @@ struct GatherParams {
   const float4* trig_g;
   const uint8_t* rot_g;
   int32_t T, n_t, dtype;
+  Paging pg;
 };
 
 struct RephaseParams {
@@ -142,6 +158,7 @@ struct RephaseParams {
   int32_t n_t, dtype;
   int32_t h_lo, h_hi;      // frames the table covers
   int32_t* status;
+  Paging pg;
 };
 
 // Snapshot / restore of the cache's non-derivable state to / from a host image (layout documented in dcp.h).
@@ -169,8 +186,8 @@ struct SnapParams {
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s);
 cudaError_t launch_snapshot(const SnapParams& p, cudaStream_t s);
-cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch);
-cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch);
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch, bool paged);
+cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch, bool paged);
 int sm_count();
 
 // ------------------------------------------------------------------------------------------ device helpers

@@ -21,6 +21,11 @@
 //
 // Bookkeeping folded in: the item holding the first block of a receiving plane sets its hist_len to
 // common_len + k, and the items of the lowest receiving plane append the kept frames to hist_t.
+//
+// Paged caches (block pools addressed through block tables) use the same decomposition: a thread's source and
+// destination offsets inside a plane come from the tables once per item, and a plane's base from its layer and head.
+#include <type_traits>
+
 #include "dcp_internal.cuh"
 
 namespace dcp {
@@ -31,8 +36,9 @@ namespace {
 // next plane's loads in flight while the current plane is turned and stored (measured on the full-depth step:
 // 248.5 us vs 253.2 us without the pipeline at 3 CTAs/SM; 259.2 us vs 269.9 us when every key turns; at 3 CTAs/SM
 // the pipelined form spills).
-template <int NW>
+template <int NW, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams p) {
+  using Off = typename std::conditional<PAGED, int64_t, int>::type;
   constexpr int VB = NW * 4;                      // bytes per vector
   constexpr int SLOTS = kBytesPerThread / VB;     // vectors per thread, tensor and plane
   wait_for_predecessor();
@@ -55,16 +61,20 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
   const int ppv = p.dtype == DCP_BF16 ? VB / 4 : VB / 8;   // rotary pairs per vector
   const int temporal_vecs = (p.n_t + ppv - 1) / ppv;
   const int row_in_slot = threadIdx.x / vpr, lane_in_row = threadIdx.x - row_in_slot * vpr;
-  const int64_t src_slot = p.src_row0 * (int64_t)p.row_bytes;
+  const int64_t src_slot = PAGED ? 0 : p.src_row0 * (int64_t)p.row_bytes;
+  auto plane_base = [&](int pl) -> int64_t {
+    if (PAGED) return (int64_t)(pl / p.pg.H) * p.pg.s_layer + (int64_t)(pl % p.pg.H) * p.pg.s_head;
+    return (int64_t)pl * p.plane_bytes;
+  };
 
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int jb = it % nblk, r = it / nblk;
     const int p0 = r * ppr, p1 = min(p.n_planes, p0 + ppr);
     const int j0 = jb * rows_per_item, nrows = min(rows_per_item, k - j0);
-    const int64_t dst_block = (p.dst_row0 + common + j0) * (int64_t)p.row_bytes;
+    const int64_t dst_block = PAGED ? 0 : (p.dst_row0 + common + j0) * (int64_t)p.row_bytes;
 
-    int src_rel[SLOTS];  // source vector inside the leaving chunk's rows, -1 if the slot is unused
-    int dst_rel[SLOTS];  // destination vector inside the block's contiguous destination rows
+    Off src_rel[SLOTS];  // source vector inside the leaving chunk's rows, -1 if the slot is unused
+    Off dst_rel[SLOTS];  // destination vector inside the block's contiguous destination rows (paged: in the plane)
     int rot[SLOTS];      // (frame << 16) | vector for a key vector the frame's table turns, -1 if it is only copied
 #pragma unroll
     for (int u = 0; u < SLOTS; ++u) {
@@ -76,8 +86,16 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
       if (row_in_slot < rows_per_slot && row < nrows) {
         const int s = __ldg(p.idx + j0 + row);
         const int f = s / p.T;
-        src_rel[u] = s * p.row_bytes + vec * VB;
-        dst_rel[u] = row * p.row_bytes + vec * VB;
+        if (PAGED) {
+          const int64_t pos = common + j0 + row;
+          src_rel[u] = (int64_t)__ldg(p.pg.src_blocks + s / p.pg.bs) * p.pg.s_block +
+                       (int64_t)(s % p.pg.bs) * p.pg.s_row + vec * VB;
+          dst_rel[u] = (int64_t)__ldg(p.pg.hist_blocks + pos / p.pg.bs) * p.pg.s_block +
+                       (pos % p.pg.bs) * p.pg.s_row + vec * VB;
+        } else {
+          src_rel[u] = s * p.row_bytes + vec * VB;
+          dst_rel[u] = row * p.row_bytes + vec * VB;
+        }
         if (vec < temporal_vecs && __ldg(p.rot_g + f)) rot[u] = (f << 16) | vec;
         if (vec == 0 && first_dyn >= p0 && first_dyn < p1) p.hist_t[common + j0 + row] = p.evict_first_frame + f;
       }
@@ -93,8 +111,8 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
 #pragma unroll
       for (int u = 0; u < SLOTS; ++u)
         if (src_rel[u] >= 0) {
-          ld_stream(ck[u], p.k + pl * p.plane_bytes + src_slot + src_rel[u]);
-          ld_stream(cv[u], p.v + pl * p.plane_bytes + src_slot + src_rel[u]);
+          ld_stream(ck[u], p.k + plane_base(pl) + src_slot + src_rel[u]);
+          ld_stream(cv[u], p.v + plane_base(pl) + src_slot + src_rel[u]);
         }
     }
     while (pl < p1) {
@@ -104,16 +122,16 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
 #pragma unroll
         for (int u = 0; u < SLOTS; ++u)
           if (src_rel[u] >= 0) {
-            ld_stream(nk[u], p.k + nx * p.plane_bytes + src_slot + src_rel[u]);
-            ld_stream(nv[u], p.v + nx * p.plane_bytes + src_slot + src_rel[u]);
+            ld_stream(nk[u], p.k + plane_base(nx) + src_slot + src_rel[u]);
+            ld_stream(nv[u], p.v + plane_base(nx) + src_slot + src_rel[u]);
           }
       }
 #pragma unroll
       for (int u = 0; u < SLOTS; ++u)
         if (rot[u] >= 0)
           dev_rotate_vec(ck[u], p.dtype, (rot[u] & 0xFFFF) * ppv, p.n_t, p.trig_g + (rot[u] >> 16) * p.n_t);
-      char* kb = p.k + pl * p.plane_bytes;
-      char* vb = p.v + pl * p.plane_bytes;
+      char* kb = p.k + plane_base(pl);
+      char* vb = p.v + plane_base(pl);
 #pragma unroll
       for (int u = 0; u < SLOTS; ++u) {
         if (src_rel[u] >= 0) {
@@ -132,11 +150,11 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
   }
 }
 
-template <int NW>
+template <int NW, bool PAGED>
 cudaError_t launch_gather_w(const GatherParams& p, cudaStream_t s, bool overlap_launch) {
   static int blocks_per_sm = 0;
   if (!blocks_per_sm) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, gather_kernel<NW>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, gather_kernel<NW, PAGED>, kThreads, 0) !=
             cudaSuccess ||
         blocks_per_sm < 1)
       blocks_per_sm = 1;
@@ -151,13 +169,15 @@ cudaError_t launch_gather_w(const GatherParams& p, cudaStream_t s, bool overlap_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_launch ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gather_kernel<NW>, p);
+  return cudaLaunchKernelEx(&cfg, gather_kernel<NW, PAGED>, p);
 }
 
 }  // namespace
 
-cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch) {
-  return p.vb == 32 ? launch_gather_w<8>(p, s, overlap_launch) : launch_gather_w<4>(p, s, overlap_launch);
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch, bool paged) {
+  if (paged)
+    return p.vb == 32 ? launch_gather_w<8, true>(p, s, overlap_launch) : launch_gather_w<4, true>(p, s, overlap_launch);
+  return p.vb == 32 ? launch_gather_w<8, false>(p, s, overlap_launch) : launch_gather_w<4, false>(p, s, overlap_launch);
 }
 
 }  // namespace dcp

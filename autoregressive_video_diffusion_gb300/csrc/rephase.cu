@@ -13,7 +13,9 @@
 // loaded into registers once per item and reused for every plane.  Planes are taken four at a time, so four
 // independent loads are in flight per thread.  Rows whose frame does not move, and rows past a plane's own history
 // length, are skipped.  The kernel runs before the gather of the same step, so hist_len still holds the lengths
-// before the step.
+// before the step.  Paged caches look a row's block up in the history block table once per item.
+#include <type_traits>
+
 #include "dcp_internal.cuh"
 
 namespace dcp {
@@ -22,8 +24,9 @@ namespace {
 
 constexpr int kPlanesInFlight = 4;
 
-template <int NW>
+template <int NW, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 3) rephase_kernel(const RephaseParams p) {
+  using Off = typename std::conditional<PAGED, int64_t, int>::type;
   constexpr int VB = NW * 4;
   wait_for_predecessor();
   allow_dependents();
@@ -40,7 +43,11 @@ __global__ void __launch_bounds__(kThreads, 3) rephase_kernel(const RephaseParam
   const int ppr = (p.n_planes + ranges - 1) / ranges;
   const int items = nblk * ranges;
   const int row_in_item = threadIdx.x / p.nvt, vec = threadIdx.x - row_in_item * p.nvt;
-  const int64_t hist0 = p.hist_row0 * (int64_t)p.row_bytes;
+  const int64_t hist0 = PAGED ? 0 : p.hist_row0 * (int64_t)p.row_bytes;
+  auto plane_base = [&](int pl) -> int64_t {
+    if (PAGED) return (int64_t)(pl / p.pg.H) * p.pg.s_layer + (int64_t)(pl % p.pg.H) * p.pg.s_head;
+    return (int64_t)pl * p.plane_bytes;
+  };
 
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int jb = it % nblk, r = it / nblk;
@@ -64,7 +71,13 @@ __global__ void __launch_bounds__(kThreads, 3) rephase_kernel(const RephaseParam
       }
     }
     if (!__syncthreads_or(live)) continue;
-    const int off = row * p.row_bytes + vec * VB;
+    Off off;
+    if (PAGED)  // the table covers history rows only: look up live rows
+      off = live ? (int64_t)__ldg(p.pg.hist_blocks + row / p.pg.bs) * p.pg.s_block +
+                       (int64_t)(row % p.pg.bs) * p.pg.s_row + vec * VB
+                 : 0;
+    else
+      off = row * p.row_bytes + vec * VB;
 
     for (int pl = p0; pl < p1; pl += kPlanesInFlight) {
       Vec<NW> x[kPlanesInFlight];
@@ -73,24 +86,24 @@ __global__ void __launch_bounds__(kThreads, 3) rephase_kernel(const RephaseParam
       for (int q = 0; q < kPlanesInFlight; ++q) {
         const int plq = pl + q;
         go[q] = live && plq < p1 && row < __ldg(p.hist_len + min(plq, p1 - 1));
-        if (go[q]) ld_plain(x[q], p.k + plq * p.plane_bytes + hist0 + off);
+        if (go[q]) ld_plain(x[q], p.k + plane_base(plq) + hist0 + off);
       }
 #pragma unroll
       for (int q = 0; q < kPlanesInFlight; ++q) {
         if (go[q]) {
           dev_rotate_vec_regs(x[q], p.dtype, vec * ppv, p.n_t, tr);
-          st_plain(p.k + (pl + q) * p.plane_bytes + hist0 + off, x[q]);
+          st_plain(p.k + plane_base(pl + q) + hist0 + off, x[q]);
         }
       }
     }
   }
 }
 
-template <int NW>
+template <int NW, bool PAGED>
 cudaError_t launch_rephase_w(const RephaseParams& p, cudaStream_t s, bool overlap_launch) {
   static int blocks_per_sm = 0;
   if (!blocks_per_sm) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, rephase_kernel<NW>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, rephase_kernel<NW, PAGED>, kThreads, 0) !=
             cudaSuccess ||
         blocks_per_sm < 1)
       blocks_per_sm = 1;
@@ -105,13 +118,16 @@ cudaError_t launch_rephase_w(const RephaseParams& p, cudaStream_t s, bool overla
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_launch ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, rephase_kernel<NW>, p);
+  return cudaLaunchKernelEx(&cfg, rephase_kernel<NW, PAGED>, p);
 }
 
 }  // namespace
 
-cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch) {
-  return p.vb == 32 ? launch_rephase_w<8>(p, s, overlap_launch) : launch_rephase_w<4>(p, s, overlap_launch);
+cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch, bool paged) {
+  if (paged)
+    return p.vb == 32 ? launch_rephase_w<8, true>(p, s, overlap_launch)
+                      : launch_rephase_w<4, true>(p, s, overlap_launch);
+  return p.vb == 32 ? launch_rephase_w<8, false>(p, s, overlap_launch) : launch_rephase_w<4, false>(p, s, overlap_launch);
 }
 
 }  // namespace dcp

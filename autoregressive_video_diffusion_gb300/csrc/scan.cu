@@ -12,6 +12,7 @@
 //                differs": t~(t) = q0 - g(q0 - t)) in double precision, stored as float hi/lo pairs.
 //   plane checks CTAs below ceil(planes / 256) also fold 256 planes' hist_len into warp-reduced atomic maxima
 //                (receiving planes' shortest and longest history, lowest receiving plane, longest history).
+//   table checks (paged caches) CTAs below ceil(entries / 256) also check 256 block-table entries each.
 //   final CTA    the last CTA to finish (completion counter) turns the ballot words into the ordered index list
 //                with one block-wide exclusive scan of their popcounts per 256 words, decides capacity and
 //                consistency, publishes the verdict for the kernels that follow and resets the counters.  Under
@@ -152,6 +153,19 @@ __device__ void plane_checks(const ScanParams& p, int slice) {
     if (longest) atomicMax(&c->acc_rp_max, longest);
     if (bad) atomicMax(&c->acc_bad, 1);
   }
+}
+
+// Paged caches: every block-table entry the step uses must name a block of the pools.  A bad entry aborts the step
+// before anything moves (the gather and re-index kernels read the tables only after the verdict).
+__device__ void table_checks(const ScanParams& p, int slice) {
+  const int e = slice * kThreads + threadIdx.x;
+  int bad = 0;
+  if (e < p.n_tbl_a + p.n_tbl_b) {
+    const int32_t b = e < p.n_tbl_a ? p.tbl_a[e] : p.tbl_b[e - p.n_tbl_a];
+    bad = b < 0 || (int64_t)b >= p.n_blocks;
+  }
+  bad = __reduce_max_sync(kFull, bad);
+  if ((threadIdx.x & 31) == 0 && bad) atomicMax(&p.ctrl->acc_bad, 1);
 }
 
 // theta_p = base^(-p / n_t) is evaluated as exp2(log2(base) * (-p / n_t)): the same value to a few ulps of fp64,
@@ -329,6 +343,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanParams p) {
   allow_dependents();
   const int id = blockIdx.x;
   if (id < p.n_plane_slices) plane_checks(p, id);
+  if (id < p.n_tbl_slices) table_checks(p, id);
   if (id < p.n_tiles) tile_work(p, id, s_ell);
   else if (id - p.n_tiles < p.n_trig_blocks) table_work(p, id - p.n_tiles);
 
@@ -349,6 +364,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanParams p) {
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
   int grid = p.n_tiles + p.n_trig_blocks;
   if (grid < p.n_plane_slices) grid = p.n_plane_slices;
+  if (grid < p.n_tbl_slices) grid = p.n_tbl_slices;
   if (grid < 1) grid = 1;
   scan_kernel<<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();

@@ -222,12 +222,44 @@ class FullDepthStep:
         return 3 if rephase else 2
 
 
+class PagedFullDepthStep(FullDepthStep):
+    """The same eviction on a paged copy of the cache: block pools of `block_size` positions (HND or NHD) and
+    block tables drawn as a seeded permutation of the pool's blocks."""
+
+    def __init__(self, w, block_size: int, layout: int):
+        import torch
+        super().__init__(w)
+        dcp, cfg, bs = self.dcp, self.cfg, block_size
+        C, sink = w.C, w.sink_chunks * w.C
+        n_sink, n_hist, n_win = sink // bs, w.hist_cap // bs, (w.window_chunks + 1) * C // bs
+        n_blocks = n_sink + n_hist + n_win
+        perm = torch.from_numpy(np.random.default_rng(0xB10C).permutation(n_blocks).astype(np.int32)).cuda()
+        pc = dcp.PagedKVCache(w.L, w.H, w.D, w.dtype, bs, layout, n_blocks, w.hist_cap, n_win)
+        pc.hist_blocks.copy_(perm[n_sink:n_sink + n_hist])
+        pc.window_blocks.copy_(perm[n_sink + n_hist:])
+        block, off = dcp.paged_row_map(cfg, w.hist_cap, bs, perm[:n_sink], pc.hist_blocks, pc.window_blocks)
+        dcp.paged_pack(pc.k_pool, self.cache.k, block, off, layout)
+        dcp.paged_pack(pc.v_pool, self.cache.v, block, off, layout)
+        pc.hist_len.copy_(self.cache.hist_len)
+        pc.hist_t.copy_(self.cache.hist_t)
+        self.cache = pc  # the contiguous tensors are released here
+        self.ws = dcp.new_workspace(dcp.dcp_paged_workspace_size(pc, cfg))
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    def step(self, x0=None, xr=None, kept_host=None):
+        w = self.w
+        self.dcp.dcp_paged_prune_step(self.cache, self.cfg, self.x0 if x0 is None else x0,
+                                      self.xr if xr is None else xr, w.slot_of(self.c), w.first_frame(self.c),
+                                      self.q0_prev, self.q0, None, self.kept, kept_host, self.ws)
+
+
 def run_gpu(w, steps: int, warmup: int, world: int, rank: int, local: int, clocks: ClockSampler | None,
-            e2e_steps: int, preroll_s: float = 1.0, keep_rule: int = 0):
+            e2e_steps: int, preroll_s: float = 1.0, keep_rule: int = 0, paged=None):
     import torch
 
     import autoregressive_video_diffusion_gb300 as dcp
-    s = FullDepthStep(w, keep_rule=keep_rule, random_seed=0x5EED)
+    s = FullDepthStep(w, keep_rule=keep_rule, random_seed=0x5EED) if paged is None else PagedFullDepthStep(w, *paged)
     stream = torch.cuda.current_stream()
     ev_scan, ev_gather = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev_scan.record(stream)
@@ -751,6 +783,17 @@ def main():
             "GB_per_s": r3["alg_bytes"] / (r3["ms_max"] * 1e-3) / 1e9, "scan_us": r3["scan_ms"] * 1e3,
             "gather_us": r3["gather_ms"] * 1e3,
             "note": "Random at the discrepancy rule's kept count (radix select of SplitMix64 priorities in the scan)"}
+        import autoregressive_video_diffusion_gb300 as dcp
+        for name, wl, layout in (("full_depth_paged_hnd", FULL, dcp.DCP_PAGED_HND),
+                                 ("full_depth_paged_nhd", FULL, dcp.DCP_PAGED_NHD),
+                                 ("full_depth_rotated_paged_hnd", FULL_ROTATED, dcp.DCP_PAGED_HND)):
+            rp = run_gpu(wl, max(5, args.steps // 2), args.warmup, world, rank, local, None, e2e_steps=0,
+                         paged=(16, layout))
+            extra[name] = {"workload": wl.name, "block_size": 16, "layout": "HND" if layout == 0 else "NHD",
+                           "kept": rp["k"], "us_per_step": rp["ms_max"] * 1e3,
+                           "GB_per_s": rp["alg_bytes"] / (rp["ms_max"] * 1e-3) / 1e9,
+                           "gather_us": rp["gather_ms"] * 1e3,
+                           "gather_GB_per_s": rp["gather_bytes"] / (rp["gather_ms"] * 1e-3) / 1e9}
         from synth.workloads import HS_PREFIX, MID, ROLLOUT, TINY
         extra["tiny_fp32_single_prune"] = run_last_eviction(TINY, reps=20)
         extra["mid_bf16_single_eviction"] = run_last_eviction(MID, reps=20)

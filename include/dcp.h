@@ -178,6 +178,50 @@ dcp_status dcp_prune_step_noalloc(const dcp_cache* cache, const dcp_config* cfg,
                                   int32_t* kept_host_pinned, void* stream);
 
 /* ---------------------------------------------------------------------------------------------------------------
+ * Paged variant: the same prune step on a cache kept in block pools addressed through block tables, the layout of
+ * paged serving stacks.  The method is unchanged (section "how it works": the kept K[m], V[m] are physically moved
+ * into the history, shortening the real KV sequence); only where a row lives differs.
+ *   pool layout DCP_PAGED_HND: k_pool, v_pool are [L][n_blocks][H][block_size][D] (one pool per layer, each block
+ *               holding block_size consecutive positions of every head, head-major inside the block);
+ *   pool layout DCP_PAGED_NHD: [L][n_blocks][block_size][H][D] (position-major inside the block).
+ * Position i of the history of plane (l, h) is row i % block_size of block hist_blocks[i / block_size] in layer
+ * l's pool, head h; position n of ring slot s is row n % block_size of block
+ * window_blocks[s * C / block_size + n / block_size].  One table serves every layer and head (a block id names
+ * the same block in each layer's pool).  The sink is never touched by a prune step, so its table is not needed
+ * here.  The caller owns the tables and the pools and must give the history, the ring slots and the sink distinct
+ * blocks.  Table entries outside [0, n_blocks) are found by the scan kernel before anything moves: the step then
+ * records DCP_EDEVICE and leaves the cache as it was.
+ * --------------------------------------------------------------------------------------------------------------- */
+#define DCP_PAGED_HND 0
+#define DCP_PAGED_NHD 1
+
+typedef struct dcp_paged_cache {
+  void* k_pool;                /* device, 16-byte aligned; D * element size a multiple of 16 */
+  void* v_pool;
+  int32_t L, H, D, dtype;
+  int32_t block_size;          /* positions per block; C and hist_cap are multiples of it */
+  int32_t layout;              /* DCP_PAGED_HND or DCP_PAGED_NHD */
+  int64_t n_blocks;            /* blocks in each layer's pool */
+  int64_t hist_cap;            /* history positions covered by hist_blocks */
+  const int32_t* hist_blocks;  /* device [hist_cap / block_size] */
+  const int32_t* window_blocks;/* device [(window_chunks + 1) * C / block_size] */
+  int32_t* hist_len;           /* device [L*H], in/out */
+  int32_t* hist_t;             /* device [hist_cap], in/out */
+  int32_t* status;             /* device, one int32 */
+} dcp_paged_cache;
+
+/* Workspace bytes of dcp_paged_prune_step for this cache/config (0 if either is invalid). */
+size_t dcp_paged_workspace_size(const dcp_paged_cache* cache, const dcp_config* cfg);
+
+/* dcp_prune_step on a paged cache: same arguments, results and errors, plus DCP_EDEVICE for a table entry outside
+ * [0, n_blocks) (checked before anything moves) and DCP_EINVAL for a block size that does not divide C or hist_cap
+ * or an unknown layout. */
+dcp_status dcp_paged_prune_step(const dcp_paged_cache* cache, const dcp_config* cfg, const float* x0hat_dev,
+                                const float* xref_dev, int32_t d, int32_t evict_slot, int32_t evict_first_frame,
+                                int32_t q0_prev, int32_t q0, const uint8_t* head_is_static_dev, int32_t* kept_dev,
+                                int32_t* kept_host_pinned, void* workspace_dev, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------------------
  * Host snapshot and restore of the pruned cache.
  * Page "기술 요약: 생성형 월드 모델을 위한 지속적 계산 상태" (gist.science/ko/paper/2607.21686), section "PCS contract":
  * a checkpoint / restore pair where restore gives back the state (round trip) and the checkpoint holds exactly the
@@ -254,6 +298,9 @@ dcp_status dcp_set_phase_events(void* ev_after_scan, void* ev_after_gather);
 
 /* ABI check for bindings: (sizeof(dcp_cache) << 16) | sizeof(dcp_config). */
 uint32_t dcp_abi_struct_sizes(void);
+
+/* ABI check for bindings: sizeof(dcp_paged_cache). */
+uint32_t dcp_abi_paged_cache_size(void);
 
 
 #ifdef __cplusplus

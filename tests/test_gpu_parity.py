@@ -294,7 +294,9 @@ def test_one_workspace_serves_every_entry_point(gpu):
 
 
 # ------------------------------------------------------------------------------------------ full-size single eviction
-def _full_size_eviction(w, sample_planes):
+def _full_size_eviction(w, sample_planes, paged=None):
+    """Full-size eviction on the GPU; paged = (block_size, layout) runs it on a paged copy of the cache (read back
+    into the contiguous cache for the checks)."""
     c, q0_prev, q0 = w.evictions()[-1]
     stream = torch.cuda.current_stream().cuda_stream
     dev = dcp.KVCache(w.L, w.H, w.D, w.dtype, w.cap, w.hist_cap)
@@ -306,8 +308,21 @@ def _full_size_eviction(w, sample_planes):
     ws = dcp.new_workspace(dcp.dcp_workspace_size(dev, gcfg))
     x0, xr = w.score_inputs(c)
     kept = torch.zeros(1, dtype=torch.int32, device="cuda")
-    dcp.dcp_prune_step(dev, gcfg, _cuda(x0), _cuda(xr), w.slot_of(c), w.first_frame(c), q0_prev, q0, None, kept, None,
-                       ws)
+    if paged:
+        from tests.paged import PagedCopy
+        pc = PagedCopy(dev, gcfg, paged[0], paged[1], seed=7)
+        pws = dcp.new_workspace(dcp.dcp_paged_workspace_size(pc.cache, gcfg))
+        dcp.dcp_paged_prune_step(pc.cache, gcfg, _cuda(x0), _cuda(xr), w.slot_of(c), w.first_frame(c), q0_prev, q0,
+                                 None, kept, None, pws)
+        assert dcp.dcp_get_status(pc.cache.status) == dcp.DCP_OK
+        assert pc.free_blocks_untouched()
+        pc.unpack_into(dev)
+        ws = pws
+        del pc
+        torch.cuda.empty_cache()
+    else:
+        dcp.dcp_prune_step(dev, gcfg, _cuda(x0), _cuda(xr), w.slot_of(c), w.first_frame(c), q0_prev, q0, None, kept,
+                           None, ws)
     assert dcp.dcp_get_status(dev.status) == dcp.DCP_OK
     ell = oracle.score(x0, xr)
     mask = oracle.keep(ell, w.gamma)
