@@ -42,7 +42,7 @@ class OracleConfig(ctypes.Structure):
                 ("window_chunks", ctypes.c_int32), ("tokens_per_frame", ctypes.c_int32),
                 ("frames_per_chunk", ctypes.c_int32), ("n_temporal_pairs", ctypes.c_int32),
                 ("rope_base", ctypes.c_double), ("g_recent_R", ctypes.c_double), ("g_span_S", ctypes.c_double),
-                ("g_mode", ctypes.c_int32), ("random_seed", ctypes.c_uint32)]
+                ("g_mode", ctypes.c_int32), ("random_seed", ctypes.c_uint32), ("reindex_mode", ctypes.c_int32)]
 
 
 _lib = None
@@ -75,6 +75,7 @@ def lib():
             "oracle_rope_reindex": ([pc, pcfg, i32, i32], i32),
             "oracle_prune_step": ([pc, pcfg, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp], i32),
             "oracle_pr_chunk": ([vp, i64, i64, i64, i64, vp, vp], None),
+            "oracle_read_history_keys": ([pc, pcfg, i32, vp], None),
             "oracle_snapshot_size": ([pc, pcfg, ctypes.c_uint32], i64),
             "oracle_snapshot": ([pc, pcfg, ctypes.c_uint32, i32, vp, i64], i32),
             "oracle_restore": ([pc, pcfg, vp, i64, vp, vp], i32),
@@ -109,11 +110,12 @@ class Cfg:
     g_span_S: float = 24.0
     g_mode: int = 0
     random_seed: int = 0
+    reindex_mode: int = 0
 
     def c(self) -> OracleConfig:
         return OracleConfig(self.gamma, self.keep_rule, self.sink_chunks, self.window_chunks, self.tokens_per_frame,
                             self.frames_per_chunk, self.n_temporal_pairs, self.rope_base, self.g_recent_R,
-                            self.g_span_S, self.g_mode, self.random_seed)
+                            self.g_span_S, self.g_mode, self.random_seed, self.reindex_mode)
 
     def random_stream(self, evict_first_frame: int) -> int:
         """The SplitMix64 stream a prune step of the Random ablation (keep_rule 2) draws from."""
@@ -267,3 +269,13 @@ def restore(cache: HostCache, cfg: Cfg, image: np.ndarray):
     rc = lib().oracle_restore(ctypes.byref(cc), ctypes.byref(oc), _p(img), img.shape[0], ctypes.byref(q0),
                               ctypes.byref(live))
     return rc, q0.value, live.value
+
+
+def read_history_keys(cache: HostCache, cfg: Cfg, q0: int) -> np.ndarray:
+    """Keys of a read-time re-indexed cache as attention at q0 sees them: [planes][hist_cap][D] (rows past a plane's
+    history are zero)."""
+    L, H, cap, D = cache.k.shape
+    out = np.zeros((L * H, cache.hist_cap, D), cache.k.dtype)
+    cc, oc = cache.c(), cfg.c()
+    lib().oracle_read_history_keys(ctypes.byref(cc), ctypes.byref(oc), q0, _p(out))
+    return out

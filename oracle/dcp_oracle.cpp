@@ -19,6 +19,8 @@
 //     R and the oldest non-sink offset Dmax to the span end (mode 0: S is the total virtual span; mode 1: old offsets
 //     occupy (R, R + S]).
 //   * the sink keeps its phase; only history keys are re-phased; values and non-temporal dims are copied bitwise.
+//   * read-time re-index (reindex_mode 1): history keys stay at their own frame's phase and are turned to
+//     t~(t; q0) when read; a step then moves keys bitwise and re-indexes nothing.
 // Parity: every function here is pinned by tests/test_oracle_pins.py (closed forms, invariants, brute force).
 #include <algorithm>
 #include <cmath>
@@ -48,6 +50,8 @@ struct oracle_config {
   double g_recent_R, g_span_S;
   int32_t g_mode;        // 0: S is the total virtual span; 1: old offsets occupy (R, R + S]
   uint32_t random_seed;  // keep_rule 2: the prune step draws from the stream (random_seed << 32) | evict_first_frame
+  int32_t reindex_mode;  // 0: keys re-phased when stored and re-indexed every step; 1: keys kept at their own frame
+                         // and turned to t~(t; q0) when read (oracle_read_history_keys)
 };
 
 enum { ORACLE_OK = 0, ORACLE_EINVAL = 1, ORACLE_ECAPACITY = 2 };
@@ -231,7 +235,10 @@ int32_t oracle_compact_layers(oracle_cache* c, const oracle_config* cfg, int32_t
       int64_t dst = sink_rows + common + j;
       int32_t t = evict_first_frame + (int32_t)(idx[(size_t)j] / T);
       std::memcpy(row_ptr(c->v, c, p, dst), row_ptr(c->v, c, p, src), (size_t)row_bytes);
-      oracle_gather_key_row(row_ptr(c->k, c, p, src), row_ptr(c->k, c, p, dst), c, cfg, t, q0);
+      if (cfg->reindex_mode == 1)
+        std::memcpy(row_ptr(c->k, c, p, dst), row_ptr(c->k, c, p, src), (size_t)row_bytes);
+      else
+        oracle_gather_key_row(row_ptr(c->k, c, p, src), row_ptr(c->k, c, p, dst), c, cfg, t, q0);
     }
     c->hist_len[p] = (int32_t)(common + k);
   }
@@ -257,6 +264,22 @@ int32_t oracle_rope_reindex(oracle_cache* c, const oracle_config* cfg, int32_t q
     }
   }
   return ORACLE_OK;
+}
+
+// ------------------------------------------------------------------------------------------- read-time re-index
+// Keys kept at their own frame t (reindex_mode 1) reach attention with the phase t~(t; q0): each history row of
+// each plane is read, its temporal pairs turned once from t to t~(t; q0), and written to out [planes][hist_cap][D]
+// (rows past a plane's history are left as they are).  Reading from the raw key turns it once, so nothing drifts.
+void oracle_read_history_keys(const oracle_cache* c, const oracle_config* cfg, int32_t q0, void* out) {
+  const int64_t C = (int64_t)cfg->tokens_per_frame * cfg->frames_per_chunk;
+  const int64_t n_planes = (int64_t)c->L * c->H;
+  const int64_t sink_rows = (int64_t)cfg->sink_chunks * C;
+  const int64_t row_bytes = (int64_t)c->D * elem_size(c->dtype);
+  for (int64_t p = 0; p < n_planes; ++p)
+    for (int64_t j = 0; j < c->hist_len[p]; ++j) {
+      char* dst = (char*)out + (p * c->hist_cap + j) * row_bytes;
+      oracle_gather_key_row(row_ptr(c->k, c, p, sink_rows + j), dst, c, cfg, c->hist_t[j], q0);
+    }
 }
 
 // ------------------------------------------------------------------------------------------- one prune step
@@ -287,8 +310,10 @@ int32_t oracle_prune_step(oracle_cache* c, const oracle_config* cfg, const float
     else if (c->hist_len[p] != common) return ORACLE_EINVAL;
   }
   if (common >= 0 && common + k > c->hist_cap) return ORACLE_ECAPACITY;
-  int32_t rc = oracle_rope_reindex(c, cfg, q0_prev, q0);
-  if (rc != ORACLE_OK) return rc;
+  if (cfg->reindex_mode != 1) {
+    int32_t rc = oracle_rope_reindex(c, cfg, q0_prev, q0);
+    if (rc != ORACLE_OK) return rc;
+  }
   return oracle_compact_layers(c, cfg, evict_slot, evict_first_frame, mask.data(), head_is_static, q0, idx_out, k_out);
 }
 

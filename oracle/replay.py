@@ -42,25 +42,27 @@ def new_host_cache(w: Workload) -> HostCache:
     return hc
 
 
-def replay(w: Workload, hc: HostCache, evictions, head_is_static=None, placed=None):
-    """Run the oracle over a list of (chunk, q0_prev, q0) evictions, placing each newly generated chunk first."""
+def replay(w: Workload, hc: HostCache, evictions, head_is_static=None, placed=None, cfg: Cfg | None = None):
+    """Run the oracle over a list of (chunk, q0_prev, q0) evictions, placing each newly generated chunk first
+    (cfg: the method parameters, default those of the workload)."""
     placed = set() if placed is None else placed
+    cfg = cfg_of(w) if cfg is None else cfg
     for c, q0_prev, q0 in evictions:
         for cc in w.resident_window(c):
             if cc not in placed:
                 place_chunk(hc, w, cc)
                 placed.add(cc)
         x0, xr = w.score_inputs(c)
-        rc, _, _, _ = prune_step(hc, cfg_of(w), x0, xr, w.slot_of(c), w.first_frame(c), q0_prev, q0, head_is_static)
+        rc, _, _, _ = prune_step(hc, cfg, x0, xr, w.slot_of(c), w.first_frame(c), q0_prev, q0, head_is_static)
         assert rc == OK, f"oracle replay refused eviction of chunk {c}: {rc}"
     return placed
 
 
-def state_before_last(w: Workload, head_is_static=None):
+def state_before_last(w: Workload, head_is_static=None, cfg: Cfg | None = None):
     """Host cache right before the workload's last eviction, and that eviction (chunk, q0_prev, q0)."""
     ev = w.evictions()
     hc = new_host_cache(w)
-    placed = replay(w, hc, ev[:-1], head_is_static)
+    placed = replay(w, hc, ev[:-1], head_is_static, cfg=cfg)
     c = ev[-1][0]
     for cc in w.resident_window(c):
         if cc not in placed:
