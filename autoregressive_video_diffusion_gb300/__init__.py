@@ -50,7 +50,8 @@ class DcpConfigC(ctypes.Structure):
                 ("frames_per_chunk", ctypes.c_int32), ("n_temporal_pairs", ctypes.c_int32),
                 ("pair_layout", ctypes.c_int32), ("rope_base", ctypes.c_double), ("g_recent_R", ctypes.c_double),
                 ("g_span_S", ctypes.c_double), ("g_mode", ctypes.c_int32), ("rephase_sink", ctypes.c_int32),
-                ("max_frames", ctypes.c_int32), ("random_seed", ctypes.c_uint32)]
+                ("max_frames", ctypes.c_int32), ("random_seed", ctypes.c_uint32), ("reindex_mode", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class DcpPagedCacheC(ctypes.Structure):
@@ -89,6 +90,9 @@ _SIGS = {
     "dcp_paged_prune_step": ([ctypes.POINTER(DcpPagedCacheC), _pg, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
                               _vp, _vp, _sz, _vp], _i32),
     "dcp_abi_paged_cache_size": ([], ctypes.c_uint32),
+    "dcp_read_history_keys": ([_pc, _pg, _i32, _i32, _i32, _vp, _vp, _sz, _vp], _i32),
+    "dcp_paged_read_history_keys": ([ctypes.POINTER(DcpPagedCacheC), _pg, _i32, _i32, _i32, _vp, _vp, _sz, _vp],
+                                    _i32),
     "dcp_snapshot_max_bytes": ([_pc, _pg, ctypes.c_uint32], _sz),
     "dcp_snapshot": ([_pc, _pg, ctypes.c_uint32, _i32, _vp, _sz, _vp, _sz, _vp], _i32),
     "dcp_restore": ([_pc, _pg, _vp, _sz, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_uint32), _vp, _sz, _vp],
@@ -151,6 +155,7 @@ class Config:
     pair_layout: int = 0
     rephase_sink: int = 0
     random_seed: int = 0
+    reindex_mode: int = 0
 
     @property
     def C(self) -> int:
@@ -160,7 +165,7 @@ class Config:
         return DcpConfigC(self.gamma, self.keep_rule, self.sink_chunks, self.window_chunks, self.tokens_per_frame,
                           self.frames_per_chunk, self.n_temporal_pairs, self.pair_layout, self.rope_base,
                           self.g_recent_R, self.g_span_S, self.g_mode, self.rephase_sink, self.max_frames,
-                          self.random_seed & 0xFFFFFFFF)
+                          self.random_seed & 0xFFFFFFFF, self.reindex_mode, 0)
 
     def random_stream(self, evict_first_frame: int) -> int:
         """SplitMix64 seed a prune step under keep_rule 2 draws from (as dcp_prune_step forms it)."""
@@ -408,3 +413,14 @@ def paged_unpack(pool: torch.Tensor, block: torch.Tensor, off: torch.Tensor, lay
     if layout == DCP_PAGED_HND:
         return pool[:, block, :, off, :].permute(1, 2, 0, 3).contiguous()
     return pool[:, block, off].permute(0, 2, 1, 3).contiguous()
+
+
+# ------------------------------------------------------------------------------------------ read-time re-index
+def dcp_read_history_keys(cache, cfg: Config, q0: int, plane0: int, n_planes: int, out: torch.Tensor,
+                          ws: torch.Tensor, stream=None) -> None:
+    """History keys of planes [plane0, plane0 + n_planes) turned to t~(t; q0) into out [n_planes][hist_cap][D]
+    (reindex_mode 1).  `cache` is a KVCache or a PagedKVCache."""
+    cc, gc = cache.c(), cfg.c()
+    fn = lib.dcp_paged_read_history_keys if isinstance(cache, PagedKVCache) else lib.dcp_read_history_keys
+    _check(fn(ctypes.byref(cc), ctypes.byref(gc), q0, plane0, n_planes, _ptr(out), _ptr(ws), ws.numel(),
+              _stream(stream)), "dcp_read_history_keys")

@@ -10,7 +10,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdcp.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
-SOURCES = ["scan.cu", "gather.cu", "rephase.cu", "snapshot.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["scan.cu", "gather.cu", "rephase.cu", "read.cu", "snapshot.cu", "api.cu", "noalloc.cu"]
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC"]
 
 

@@ -45,6 +45,7 @@ dcp_status check_cache_cfg(const dcp_cache* c, const dcp_config* g, Derived* d) 
   if (g->g_mode == 0 && g->g_span_S < g->g_recent_R) return DCP_EINVAL;
   if (g->g_mode == 1 && g->g_span_S < 0.0) return DCP_EINVAL;
   if (g->keep_rule < 0 || g->keep_rule > 2) return DCP_EINVAL;
+  if ((g->reindex_mode != 0 && g->reindex_mode != 1) || g->reserved != 0) return DCP_EINVAL;
   if (!std::isfinite(g->gamma)) return DCP_EINVAL;
   if (g->max_frames < 1) return DCP_EINVAL;
   if (c->hist_cap < 0 || c->hist_cap > INT32_MAX) return DCP_EINVAL;
@@ -104,6 +105,7 @@ ScanParams cache_scan_params(const dcp_cache* c, const dcp_config* g, const Deri
   ScanParams sp{};
   sp.gamma = g->gamma;
   sp.keep_rule = g->keep_rule;
+  sp.g_identity = g->reindex_mode == 1 ? 1 : 0;
   sp.ctrl = at<Ctrl>(ws, 0);
   sp.bits = at<uint32_t>(ws, d.lay.bits);
   sp.status = c->status;
@@ -276,6 +278,61 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
                            int32_t q0_prev, int32_t q0, const uint8_t* head_is_static, int32_t* kept_dev,
                            int32_t* kept_host_pinned, void* ws, size_t ws_bytes, void* stream);
 
+// Read-time re-index: the scan kernel's table CTAs build the turn t -> t~(t; q0) for frames [T_s, q0) and its plane
+// checks find the longest history; the read kernel follows on the stream.
+dcp_status read_impl(const dcp_cache* cache, const PagedView* pv, const dcp_config* cfg, int32_t q0, int32_t plane0,
+                     int32_t n_planes, void* out, void* ws, size_t ws_bytes, void* stream) {
+  Derived d;
+  if (check_cache_cfg(cache, cfg, &d) != DCP_OK || cfg->reindex_mode != 1) return DCP_EINVAL;
+  if (q0 < d.T_s || q0 > cfg->max_frames) return DCP_EINVAL;
+  if (plane0 < 0 || n_planes < 1 || (int64_t)plane0 + n_planes > d.n_planes) return DCP_EINVAL;
+  if (!out || !aligned(out, 16) || check_ws(ws, ws_bytes, d.lay.total) != DCP_OK) return DCP_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  ScanParams sp = cache_scan_params(cache, cfg, d, ws);
+  sp.g_identity = 0;
+  sp.want_rephase = 1;
+  sp.evict_first_frame = d.T_s;
+  sp.g_frames = q0 - d.T_s;
+  sp.trig_g = at<float4>(ws, d.lay.trig_h);
+  sp.rot_g = at<uint8_t>(ws, d.lay.rot_h);
+  sp.h_lo = sp.h_hi = d.T_s;
+  sp.q0 = q0;
+  sp.q0_prev = q0;
+  finish_tables(sp);
+  ReadParams rp{};
+  rp.k = static_cast<char*>(cache->k);
+  rp.row_bytes = cache->D * d.esize;
+  rp.plane_bytes = cache->cap * (int64_t)rp.row_bytes;
+  rp.vb = (vector_bytes(cache, rp.row_bytes) == 32 && aligned(out, 32)) ? 32 : 16;
+  rp.nvt = (2 * cfg->n_temporal_pairs * d.esize + rp.vb - 1) / rp.vb;
+  rp.vpr = rp.row_bytes / rp.vb;
+  rp.hist_row0 = d.sink_rows;
+  rp.plane0 = plane0;
+  rp.n_planes = n_planes;
+  rp.hist_cap = cache->hist_cap;
+  rp.out = static_cast<char*>(out);
+  rp.ctrl = at<Ctrl>(ws, 0);
+  rp.hist_len = cache->hist_len;
+  rp.hist_t = cache->hist_t;
+  rp.trig = sp.trig_g;
+  rp.rot = sp.rot_g;
+  rp.f_lo = d.T_s;
+  rp.f_hi = q0;
+  rp.n_t = cfg->n_temporal_pairs;
+  rp.dtype = cache->dtype;
+  rp.status = cache->status;
+  if (pv) {
+    rp.pg = pv->pg;
+    sp.tbl_a = pv->pg.hist_blocks;
+    sp.n_tbl_a = (int32_t)(cache->hist_cap / pv->pg.bs);
+    sp.n_blocks = pv->n_blocks;
+    sp.n_tbl_slices = (sp.n_tbl_a + kThreads - 1) / kThreads;
+  }
+  dcp_status rc = cuda_ok(launch_scan(sp, st));
+  if (rc != DCP_OK) return rc;
+  return cuda_ok(launch_read(rp, st, pv != nullptr));
+}
+
 SnapParams snap_params(const dcp_cache* c, const dcp_config* g, const Derived& d, uint32_t live_slots, int n_live,
                        char* img_dev, size_t img_bytes, void* ws, int dir) {
   SnapParams p{};
@@ -408,7 +465,8 @@ dcp_status dcp_rope_reindex(const dcp_cache* cache, const dcp_config* cfg, int32
   if (check_cache_cfg(cache, cfg, &d) != DCP_OK) return DCP_EINVAL;
   if (q0_prev > q0 || q0 > cfg->max_frames || q0_prev < d.T_s) return DCP_EINVAL;
   if (check_ws(ws, ws_bytes, d.lay.total) != DCP_OK) return DCP_EINVAL;
-  if (q0_prev == q0 || cfg->n_temporal_pairs == 0) return DCP_OK;  // no key changes phase
+  // no key changes phase (or, with read-time re-index, keys keep their own frame's phase)
+  if (q0_prev == q0 || cfg->n_temporal_pairs == 0 || cfg->reindex_mode == 1) return DCP_OK;
   cudaStream_t st = (cudaStream_t)stream;
   ScanParams sp = cache_scan_params(cache, cfg, d, ws);
   sp.want_rephase = 1;
@@ -450,6 +508,20 @@ dcp_status dcp_paged_prune_step(const dcp_paged_cache* cache, const dcp_config* 
 
 uint32_t dcp_abi_paged_cache_size(void) { return (uint32_t)sizeof(dcp_paged_cache); }
 
+dcp_status dcp_read_history_keys(const dcp_cache* cache, const dcp_config* cfg, int32_t q0, int32_t plane0,
+                                 int32_t n_planes, void* out_dev, void* ws, size_t ws_bytes, void* stream) {
+  return read_impl(cache, nullptr, cfg, q0, plane0, n_planes, out_dev, ws, ws_bytes, stream);
+}
+
+dcp_status dcp_paged_read_history_keys(const dcp_paged_cache* cache, const dcp_config* cfg, int32_t q0,
+                                       int32_t plane0, int32_t n_planes, void* out_dev, void* ws, size_t ws_bytes,
+                                       void* stream) {
+  dcp_cache shadow;
+  PagedView pv;
+  if (paged_view(cache, cfg, &shadow, &pv) != DCP_OK) return DCP_EINVAL;
+  return read_impl(&shadow, &pv, cfg, q0, plane0, n_planes, out_dev, ws, ws_bytes, stream);
+}
+
 }  // extern "C"
 
 namespace {
@@ -466,7 +538,7 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
   if (kept_dev && !aligned(kept_dev, 4)) return DCP_EINVAL;
   if (check_ws(ws, ws_bytes, d.lay.total) != DCP_OK) return DCP_EINVAL;
   cudaStream_t st = (cudaStream_t)stream;
-  const bool rephase = q0_prev != q0 && cfg->n_temporal_pairs > 0;
+  const bool rephase = q0_prev != q0 && cfg->n_temporal_pairs > 0 && cfg->reindex_mode == 0;
   ScanParams sp = cache_scan_params(cache, cfg, d, ws);
   sp.x0hat = x0hat;
   sp.xref = xref;

@@ -95,8 +95,9 @@ struct ScanParams {
   int32_t n_trig_blocks;
   float4* trig_g;          // [F][n_t]: turn from t to t~(t; q0) for the leaving chunk's frames
   uint8_t* rot_g;          // [F]: nonzero if that frame turns at all
-  int32_t g_frames;        // F, or 0 when no gather follows
+  int32_t g_frames;        // F, or 0 when no gather follows (read-time re-index: frames [T_s, q0))
   int32_t evict_first_frame;
+  int32_t g_identity;      // read-time re-index mode: moved keys keep their phase (the trig_g turns are zero)
   float4* trig_h;          // [max_frames][n_t]: turn from t~(t; q0_prev) to t~(t; q0)
   uint8_t* rot_h;          // [max_frames]
   int32_t h_lo, h_hi;      // frames [h_lo, h_hi) of the history table (empty when no re-index follows)
@@ -184,7 +185,31 @@ struct SnapParams {
   int32_t* status;
 };
 
+// Read-time re-index: history keys turned from their own frame t to t~(t; q0) into a contiguous output.
+struct ReadParams {
+  char* k;
+  int64_t plane_bytes;
+  int32_t row_bytes;
+  int32_t vb;              // bytes per vector (16 or 32)
+  int32_t nvt;             // vectors of a row that hold temporal pairs
+  int32_t vpr;             // vectors per row
+  int64_t hist_row0;       // sink_rows
+  int32_t plane0, n_planes;
+  int64_t hist_cap;        // output rows per plane
+  char* out;               // [n_planes][hist_cap][D]
+  const Ctrl* ctrl;
+  const int32_t* hist_len;
+  const int32_t* hist_t;
+  const float4* trig;      // [frames][n_t]: turn from t to t~(t; q0), frames from f_lo
+  const uint8_t* rot;
+  int32_t f_lo, f_hi;
+  int32_t n_t, dtype;
+  int32_t* status;
+  Paging pg;
+};
+
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s);
+cudaError_t launch_read(const ReadParams& p, cudaStream_t s, bool paged);
 cudaError_t launch_snapshot(const SnapParams& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch, bool paged);
 cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch, bool paged);

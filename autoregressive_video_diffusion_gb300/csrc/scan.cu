@@ -179,7 +179,8 @@ __device__ void table_work(const ScanParams& p, int block) {
   if (e < n_g) {
     const int f = e / p.n_t, pp = e - f * p.n_t;
     const double t = (double)(p.evict_first_frame + f);
-    const double delta = __dsub_rn(dev_phase(t, (double)p.q0, (double)p.T_s, p.R, p.S, p.g_mode), t);
+    const double delta =
+        p.g_identity ? 0.0 : __dsub_rn(dev_phase(t, (double)p.q0, (double)p.T_s, p.R, p.S, p.g_mode), t);
     const double theta = exp2(__dmul_rn(-(double)pp / (double)p.n_t, log2_base));
     p.trig_g[e] = dev_trig_entry(__dmul_rn(theta, delta));
     if (pp == 0) p.rot_g[f] = delta != 0.0;

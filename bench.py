@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one full-depth gather launch from the ncu capture summarised in
 # profiles/gather_kernel_full_depth_dram.md.  They describe the kernel sources they were taken on: when the hash of
 # those sources differs, the bench reports no traffic figure.
-GATHER_TRAFFIC_BYTES = 1_500_011_008
-GATHER_TRAFFIC_SOURCES_SHA256 = "c90929ee4c7a38817c706c35694c9a7e2faab07cf5dfd534e8081ad5b8834434"
+GATHER_TRAFFIC_BYTES = 1_502_524_160
+GATHER_TRAFFIC_SOURCES_SHA256 = "7946fea54c372ea1e90cd9e7753813f1c4fc34f72fb40962a66f848ff7daed41"
 
 
 def _gather_traffic():
@@ -361,12 +361,13 @@ class DeviceRollout:
     chunk's K/V is written on the device by the seeded generator and its score inputs staged (untimed), then the prune
     step runs.  Used for the workloads whose history matters (mid eviction, head-specialised prefix pass, rollout)."""
 
-    def __init__(self, w, head_is_static=None):
+    def __init__(self, w, head_is_static=None, reindex_mode: int = 0):
         import torch
 
         import autoregressive_video_diffusion_gb300 as dcp
         from synth import workloads as W
         self.w, self.dcp, self.W, self.torch = w, dcp, W, torch
+        self.reindex_mode = reindex_mode
         self.stream = torch.cuda.current_stream()
         self.cache = dcp.KVCache(w.L, w.H, w.D, w.dtype, w.cap, w.hist_cap)
         s = self.stream.cuda_stream
@@ -377,7 +378,7 @@ class DeviceRollout:
                               window_chunks=w.window_chunks, tokens_per_frame=w.tokens_per_frame,
                               frames_per_chunk=w.frames_per_chunk, n_temporal_pairs=w.n_temporal_pairs,
                               rope_base=w.rope_base, g_recent_R=w.R, g_span_S=w.S, g_mode=w.g_mode,
-                              max_frames=w.max_frames)
+                              max_frames=w.max_frames, reindex_mode=reindex_mode)
         self.ws = dcp.new_workspace(dcp.dcp_workspace_size(self.cache, self.cfg))
         self.static = head_is_static
         self.hs = None if head_is_static is None else torch.from_numpy(head_is_static).cuda()
@@ -420,7 +421,7 @@ class DeviceRollout:
         w = self.w
         T_s = w.sink_chunks * w.F
         end = w.S if w.g_mode == 0 else w.R + w.S
-        moves = q0 != q0_prev and (q0 - T_s > end or q0_prev - T_s > end)
+        moves = q0 != q0_prev and (q0 - T_s > end or q0_prev - T_s > end) and self.reindex_mode == 0
         return hist_len_sum if moves else 0
 
     def check(self):
@@ -488,13 +489,15 @@ def run_head_specialised(w, reps: int):
     return out
 
 
-def run_rollout(w):
+def run_rollout(w, reindex_mode: int = 0):
     """The minute-long rollout: every chunk generated in turn, a prune step after each one that leaves the window;
-    per-step times, and the cumulative PR against FullKV kept by the library's host counter."""
+    per-step times, and the cumulative PR against FullKV kept by the library's host counter.  With read-time
+    re-index (reindex_mode 1) the steps re-index nothing, and the read of the final history at the final q0
+    (dcp_read_history_keys of every plane) is timed as well."""
     import torch
 
     import autoregressive_video_diffusion_gb300 as dcp
-    r = DeviceRollout(w)
+    r = DeviceRollout(w, reindex_mode=reindex_mode)
     pr = dcp.DcpPrCounter(0, 0)
     ev = {c: (q0p, q0) for c, q0p, q0 in w.evictions()}
     steps = []
@@ -519,7 +522,27 @@ def run_rollout(w):
            "last10_GB_per_s": float(nb[-10:].sum() / (ms[-10:].sum() * 1e-3) / 1e9),
            "final_history_rows": int(r.cache.hist_len[0].item()), "cumulative_PR": dcp.dcp_pr_value(pr),
            "kept_fraction_mean": float(np.mean([s[2] for s in steps]) / w.C),
-           "curve_us": [round(float(x) * 1e3, 1) for x in ms]}
+           "curve_us": [round(float(x) * 1e3, 1) for x in ms], "reindex_mode": reindex_mode}
+    if reindex_mode == 1:
+        q0_last = w.evictions()[-1][2]
+        out_keys = torch.empty((w.n_planes, w.hist_cap, w.D), dtype=r.cache.k.dtype, device="cuda")
+        rows = int(r.cache.hist_len.sum().item())
+        times = []
+        for _ in range(5):
+            r.flush_buf.fill_(1)
+            r.drain_sum = r.drain_buf.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(r.stream)
+            dcp.dcp_read_history_keys(r.cache, r.cfg, q0_last, 0, w.n_planes, out_keys, r.ws)
+            b.record(r.stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        r.check()
+        rms = float(np.median(times))
+        nbytes = rows * w.D * w.esize * 2
+        out["read_history_keys"] = {"rows": rows, "q0": q0_last, "us": rms * 1e3, "bytes": nbytes,
+                                    "GB_per_s": nbytes / (rms * 1e-3) / 1e9}
+        del out_keys
     del r
     torch.cuda.empty_cache()
     return out
@@ -799,6 +822,7 @@ def main():
         extra["mid_bf16_single_eviction"] = run_last_eviction(MID, reps=20)
         extra["head_specialised_prefix"] = run_head_specialised(HS_PREFIX, reps=3)
         extra["minute_rollout_gqa8"] = run_rollout(ROLLOUT)
+        extra["minute_rollout_gqa8_read_time_reindex"] = run_rollout(ROLLOUT, reindex_mode=1)
         from synth.workloads import scaled
         extra["host_snapshot_restore"] = run_snapshot(scaled(FULL, L=8), reps=5)
     if rank != 0:

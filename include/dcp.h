@@ -90,6 +90,11 @@ typedef struct dcp_config {
   int32_t rephase_sink;      /* must be 0: the sink keeps its stored phase */
   int32_t max_frames;        /* largest q0 (latent frame index) the workspace is sized for */
   uint32_t random_seed;      /* keep_rule 2: a prune step draws from stream (random_seed << 32) | evict_first_frame */
+  int32_t reindex_mode;      /* 0: keys take t~(t; q0) when they enter the history and the history is re-indexed at
+                                every step (eager); 1: read-time re-index: history keys keep their own frame's phase,
+                                move bitwise, nothing is re-indexed, and dcp_read_history_keys turns them to
+                                t~(t; q0) when they are read */
+  int32_t reserved;          /* must be 0 */
 } dcp_config;
 
 /* Bytes of device workspace the cache/config need (prune, compact, re-index and score calls for this cache). */
@@ -177,6 +182,19 @@ dcp_status dcp_prune_step_noalloc(const dcp_cache* cache, const dcp_config* cfg,
                                   int32_t q0_prev, int32_t q0, const uint8_t* head_is_static_dev, int32_t* kept_dev,
                                   int32_t* kept_host_pinned, void* stream);
 
+/* Read-time re-index [differs] (reindex_mode 1): the history keys of planes [plane0, plane0 + n_planes) as attention
+ * at query frame q0 sees them.  Row j of plane p (j < hist_len[p]) is the stored key, which sits at its own frame
+ * t = hist_t[j], with each temporal pair p' turned once by theta_p' * (t~(t; q0) - t); every other dim is copied
+ * bitwise.  out_dev: [n_planes][hist_cap][D] of the cache's type (16-byte aligned); rows at or past a plane's
+ * history length are not written.  Keys are turned from their raw phase at every read, so repeated reads at moving
+ * q0 accumulate no rounding.  Two launches (phase table, then the read), no host synchronisation.
+ * Device errors: DCP_EDEVICE (a hist_len outside [0, hist_cap]: nothing is written; a history frame outside
+ * [sink frames, q0): that row is not written).
+ * Host errors: DCP_EINVAL (bad cache/config, reindex_mode != 1, q0 outside [sink frames, max_frames], plane range
+ * outside [0, L*H), null or misaligned out_dev, short workspace). */
+dcp_status dcp_read_history_keys(const dcp_cache* cache, const dcp_config* cfg, int32_t q0, int32_t plane0,
+                                 int32_t n_planes, void* out_dev, void* workspace_dev, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------------------------------------------
  * Paged variant: the same prune step on a cache kept in block pools addressed through block tables, the layout of
  * paged serving stacks.  The method is unchanged (section "how it works": the kept K[m], V[m] are physically moved
@@ -212,6 +230,11 @@ typedef struct dcp_paged_cache {
 
 /* Workspace bytes of dcp_paged_prune_step for this cache/config (0 if either is invalid). */
 size_t dcp_paged_workspace_size(const dcp_paged_cache* cache, const dcp_config* cfg);
+
+/* dcp_read_history_keys on a paged cache (history rows found through hist_blocks; entries are checked first). */
+dcp_status dcp_paged_read_history_keys(const dcp_paged_cache* cache, const dcp_config* cfg, int32_t q0,
+                                       int32_t plane0, int32_t n_planes, void* out_dev, void* workspace_dev,
+                                       size_t ws_bytes, void* stream);
 
 /* dcp_prune_step on a paged cache: same arguments, results and errors, plus DCP_EDEVICE for a table entry outside
  * [0, n_blocks) (checked before anything moves) and DCP_EINVAL for a block size that does not divide C or hist_cap

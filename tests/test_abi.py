@@ -38,7 +38,8 @@ def test_every_declared_symbol_is_exported():
 def test_struct_layout_matches_binding():
     sizes = dcp.lib.dcp_abi_struct_sizes()
     assert sizes >> 16 == ctypes.sizeof(dcp.DcpCacheC) == 72
-    assert sizes & 0xFFFF == ctypes.sizeof(dcp.DcpConfigC) == 72
+    assert sizes & 0xFFFF == ctypes.sizeof(dcp.DcpConfigC) == 80
+    assert dcp.lib.dcp_abi_paged_cache_size() == ctypes.sizeof(dcp.DcpPagedCacheC) == 96
 
 
 def test_status_strings():
@@ -93,7 +94,7 @@ def test_invalid_cache_rejected(bad):
     dict(n_temporal_pairs=65), dict(n_temporal_pairs=-1), dict(pair_layout=1), dict(rephase_sink=1),
     dict(rope_base=0.0), dict(rope_base=float("nan")), dict(g_recent_R=11.0), dict(g_span_S=11.5),
     dict(g_mode=2), dict(g_mode=1, g_span_S=-1.0), dict(keep_rule=3), dict(keep_rule=-1),
-    dict(gamma=float("inf")), dict(max_frames=0)])
+    dict(gamma=float("inf")), dict(max_frames=0), dict(reindex_mode=2), dict(reindex_mode=-1)])
 def test_invalid_config_rejected(bad):
     assert _ws_size(_cache(), _cfg(**bad)) == 0
 
