@@ -615,7 +615,10 @@ def run_entry_case(case: str, steps: int, warmup: int):
     """Single entry points on their own (one GPU), for per-kernel measurement and profiling captures:
     reindex: dcp_rope_reindex of a bf16 cache of 64 planes x 90,000 history rows (frames 4-219, ~417 rows per frame,
              D 128, n_t 22) moved from q0 220 to 224 (then 224 -> 228, ...); algorithmic bytes 2 x 88 B per row.
-    score:   dcp_score_mask of the full-depth workload's 6240 x 64 score inputs; algorithmic bytes 2 x 6240 x 64 x 4."""
+    score:   dcp_score_mask of the full-depth workload's 6240 x 64 score inputs; algorithmic bytes 2 x 6240 x 64 x 4.
+    read:    dcp_read_history_keys (read-time re-index) of the same 64-plane, 90,000-row history at q0 224, 228, ...
+             into a [64][100000][128] buffer; algorithmic bytes 2 x 256 B per row.
+    random:  dcp_score_mask under keep rule 2 (Random at the discrepancy rule's count) of the full-depth chunk."""
     import torch
 
     import __graft_entry__
@@ -624,7 +627,7 @@ def run_entry_case(case: str, steps: int, warmup: int):
     from synth.workloads import FULL
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     drain = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
-    if case == "reindex":
+    if case in ("reindex", "read"):
         L, H, D, C, hist_cap, rows = 8, 8, 128, 6240, 100000, 90000
         cache = dcp.KVCache(L, H, D, dcp.DCP_BF16, C + hist_cap + 4 * C, hist_cap)
         cache.k.normal_(generator=torch.Generator(device="cuda").manual_seed(1234))
@@ -632,13 +635,19 @@ def run_entry_case(case: str, steps: int, warmup: int):
         cache.hist_len.fill_(rows)
         frames = (4 + np.arange(rows) * 216 // rows).astype(np.int32)
         cache.hist_t[:rows].copy_(torch.from_numpy(frames))
-        cfg = dcp.Config(max_frames=1024)
+        cfg = dcp.Config(max_frames=1024, reindex_mode=1 if case == "read" else 0)
         ws = dcp.new_workspace(dcp.dcp_workspace_size(cache, cfg))
-
-        def call(i):
-            dcp.dcp_rope_reindex(cache, cfg, 220 + 4 * i, 224 + 4 * i, ws)
-        nbytes = L * H * rows * 2 * 88
         status = cache.status
+        if case == "reindex":
+            def call(i):
+                dcp.dcp_rope_reindex(cache, cfg, 220 + 4 * i, 224 + 4 * i, ws)
+            nbytes = L * H * rows * 2 * 88
+        else:
+            out = torch.empty((L * H, hist_cap, D), dtype=torch.bfloat16, device="cuda")
+
+            def call(i):
+                dcp.dcp_read_history_keys(cache, cfg, 224 + 4 * i, 0, L * H, out, ws)
+            nbytes = L * H * rows * 2 * D * 2
     else:
         c = FULL.evictions()[-1][0]
         x0, xr = (torch.from_numpy(a).cuda() for a in FULL.score_inputs(c))
@@ -648,8 +657,10 @@ def run_entry_case(case: str, steps: int, warmup: int):
         kept = torch.zeros(1, dtype=torch.int32, device="cuda")
         idx = torch.empty(n, dtype=torch.int32, device="cuda")
 
+        rule = 2 if case == "random" else 0
+
         def call(i):
-            dcp.dcp_score_mask(x0, xr, FULL.gamma, 0, None, None, idx, kept, status, ws)
+            dcp.dcp_score_mask(x0, xr, FULL.gamma, rule, None, None, idx, kept, status, ws, random_stream=i)
         nbytes = 2 * n * FULL.d * 4
     for i in range(warmup):
         call(i)
@@ -732,9 +743,10 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: the same workload with fewer layers (a few GB on the device)")
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before the timed region")
-    ap.add_argument("--case", default="step", choices=["step", "reindex", "score", "snapshot"],
+    ap.add_argument("--case", default="step", choices=["step", "reindex", "score", "random", "read", "snapshot"],
                     help="step: the prune step (default); reindex: dcp_rope_reindex of a 64-plane cache with 90,000 "
-                         "history rows per plane; score: dcp_score_mask of one full-depth chunk; snapshot: "
+                         "history rows per plane; score: dcp_score_mask of one full-depth chunk (random: under "
+                         "keep rule 2); read: dcp_read_history_keys of the re-index case's history; snapshot: "
                          "dcp_snapshot / dcp_restore of the state after the full-depth eviction cut to --layers "
                          "(default 8) layers")
     args = ap.parse_args()
