@@ -31,9 +31,11 @@ struct Ctrl {
   int32_t acc_first_inv;    // max over receiving planes of INT32_MAX - plane
   int32_t acc_rp_max;       // max over all planes of hist_len
   int32_t acc_bad;          // some plane's hist_len is outside [0, hist_cap]
+  int32_t acc_all_min_inv;  // max over all planes of INT32_MAX - hist_len
+  int32_t rp_min;           // shortest history of any plane before the step (rows below it exist in every plane)
   int64_t snap_rows;        // snapshot / restore: saved rows per tensor
   int64_t snap_data_off;    // snapshot / restore: byte offset of the K block in the image
-  int32_t pad[46];
+  int32_t pad[44];
 };
 static_assert(sizeof(Ctrl) == 256, "ctrl block is one 256-byte line");
 

@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(kThreads, 3) read_kernel(const ReadParams p) {
   const Ctrl* c = p.ctrl;
   if (c->abort) return;
   const int rp_max = c->rp_max;  // longest history of any plane
+  const int rp_min = c->rp_min;  // rows below it are history in every plane
   if (rp_max <= 0) return;
   const int ppv = p.dtype == DCP_BF16 ? VB / 4 : VB / 8;
   const int rows_per_item = kThreads / p.vpr;  // vpr <= kThreads: rows are at most 4 KiB
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 3) read_kernel(const ReadParams p) {
 #pragma unroll
       for (int q = 0; q < kPlanesInFlight; ++q) {
         const int plq = pl + q;
-        go[q] = valid && plq < p1 && row < __ldg(p.hist_len + p.plane0 + min(plq, p1 - 1));
+        go[q] = valid && plq < p1 && (row < rp_min || row < __ldg(p.hist_len + p.plane0 + min(plq, p1 - 1)));
         if (go[q]) ld_stream(x[q], p.k + plane_base(p.plane0 + plq) + hist0 + src);
       }
 #pragma unroll

@@ -123,13 +123,14 @@ __device__ void tile_work(const ScanParams& p, int tile_id, float* s_ell) {
 
 __device__ void plane_checks(const ScanParams& p, int slice) {
   const int pl = slice * kThreads + threadIdx.x;
-  int len1 = 0, min_inv = 0, first_inv = 0, longest = 0, bad = 0;
+  int len1 = 0, min_inv = 0, first_inv = 0, longest = 0, bad = 0, all_min_inv = 0;
   if (pl < p.n_planes) {
     const int len = p.hist_len[pl];
     if (len < 0 || len > p.hist_cap) {
       bad = 1;
     } else {
       longest = len;
+      all_min_inv = INT32_MAX - len;
       const bool receives = p.update_cache && !(p.head_is_static && p.head_is_static[pl]);
       if (receives) {
         len1 = len + 1;
@@ -142,6 +143,7 @@ __device__ void plane_checks(const ScanParams& p, int slice) {
   min_inv = __reduce_max_sync(kFull, min_inv);
   first_inv = __reduce_max_sync(kFull, first_inv);
   longest = __reduce_max_sync(kFull, longest);
+  all_min_inv = __reduce_max_sync(kFull, all_min_inv);
   bad = __reduce_max_sync(kFull, bad);
   if ((threadIdx.x & 31) == 0) {
     Ctrl* c = p.ctrl;
@@ -151,6 +153,7 @@ __device__ void plane_checks(const ScanParams& p, int slice) {
       atomicMax(&c->acc_first_inv, first_inv);
     }
     if (longest) atomicMax(&c->acc_rp_max, longest);
+    if (all_min_inv) atomicMax(&c->acc_all_min_inv, all_min_inv);
     if (bad) atomicMax(&c->acc_bad, 1);
   }
 }
@@ -325,12 +328,15 @@ __device__ void finalize(const ScanParams& p, int* s_warp, int* s_pick) {
     c->common_len = common;
     c->first_dyn = first;
     c->rp_max = p.want_rephase ? longest : 0;
+    const int all_min_inv = __ldcg(&c->acc_all_min_inv);
+    c->rp_min = (p.want_rephase && all_min_inv > 0 && !bad) ? INT32_MAX - all_min_inv : 0;
     c->abort = abort;
     if (p.kept_dev) *p.kept_dev = k;
     c->acc_len_max1 = 0;
     c->acc_len_min_inv = 0;
     c->acc_first_inv = 0;
     c->acc_rp_max = 0;
+    c->acc_all_min_inv = 0;
     c->acc_bad = 0;
     c->done = 0u;
   }
