@@ -53,7 +53,9 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
   const int rows_per_item = SLOTS * rows_per_slot;
   const int shift = vpr >= SLOTS ? vpr / SLOTS : 1;
   const int nblk = (k + rows_per_item - 1) / rows_per_item;
-  int ranges = (int)gridDim.x / nblk;
+  // about four items per CTA: CTAs that finish early take more work, which trims the tail (measured on the
+  // full-depth step: gather 238.9 vs 240.3 us, and 252.2 vs 256.9 us when every key turns, against one item per CTA)
+  int ranges = (int)gridDim.x * 4 / nblk;
   if (ranges < 1) ranges = 1;
   if (ranges > p.n_planes) ranges = p.n_planes;
   const int ppr = (p.n_planes + ranges - 1) / ranges;
