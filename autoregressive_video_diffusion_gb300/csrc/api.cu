@@ -196,6 +196,20 @@ dcp_status check_live(const dcp_config* g, uint32_t live_slots, int* n_live) {
   return DCP_OK;
 }
 
+// Where a kernel can read a caller's buffer: device memory as it is; page-locked host memory (cudaHostAlloc,
+// cudaHostRegister) through its device address (the kernel then reads over the host link); nullptr for memory the
+// device cannot reach (pageable host memory), which the caller gets back as DCP_EINVAL.
+const void* device_view(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+  return nullptr;
+}
+
 // Device address of a host image: page-locked host memory (cudaHostAlloc, cudaHostRegister) that the device reaches
 // through unified addressing.
 char* image_device_ptr(const void* img) {
@@ -408,6 +422,9 @@ dcp_status dcp_score_mask(const float* x0hat, const float* xref, int32_t n_tok, 
     return DCP_EINVAL;
   const Layout lay = make_layout(n_tok, 0, 0, 0, 0);
   if (check_ws(ws, ws_bytes, lay.total) != DCP_OK) return DCP_EINVAL;
+  x0hat = static_cast<const float*>(device_view(x0hat));  // device memory or page-locked host memory
+  xref = static_cast<const float*>(device_view(xref));
+  if (!x0hat || !xref) return DCP_EINVAL;
   ScanParams sp{};
   sp.x0hat = x0hat;
   sp.xref = xref;
@@ -536,7 +553,17 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
   if (q0_prev > q0 || q0_prev < d.T_s) return DCP_EINVAL;
   if (!x0hat || !xref || dd < 1 || !aligned(x0hat, 4) || !aligned(xref, 4)) return DCP_EINVAL;
   if (kept_dev && !aligned(kept_dev, 4)) return DCP_EINVAL;
+  if (kept_host_pinned && !aligned(kept_host_pinned, 4)) return DCP_EINVAL;
   if (check_ws(ws, ws_bytes, d.lay.total) != DCP_OK) return DCP_EINVAL;
+  // score rows in device memory, or in page-locked host memory read over the host link by the scan kernel
+  x0hat = static_cast<const float*>(device_view(x0hat));
+  xref = static_cast<const float*>(device_view(xref));
+  if (!x0hat || !xref) return DCP_EINVAL;
+  int32_t* kept_host = nullptr;  // page-locked: written by the scan kernel itself
+  if (kept_host_pinned) {
+    kept_host = static_cast<int32_t*>(const_cast<void*>(device_view(kept_host_pinned)));
+    if (!kept_host) return DCP_EINVAL;
+  }
   cudaStream_t st = (cudaStream_t)stream;
   const bool rephase = q0_prev != q0 && cfg->n_temporal_pairs > 0 && cfg->reindex_mode == 0;
   ScanParams sp = cache_scan_params(cache, cfg, d, ws);
@@ -550,6 +577,7 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
   sp.mask_out = at<uint8_t>(ws, d.lay.mask);
   sp.idx_out = at<int32_t>(ws, d.lay.idx);
   sp.kept_dev = kept_dev;
+  sp.kept_host = kept_host;
   sp.update_cache = 1;
   sp.want_rephase = rephase ? 1 : 0;
   sp.head_is_static = head_is_static;
@@ -587,8 +615,6 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
   rc = cuda_ok(launch_gather(gp, st, g_ev_after_scan == nullptr, pv != nullptr));
   if (rc != DCP_OK) return rc;
   if (g_ev_after_gather && cudaEventRecord(g_ev_after_gather, st) != cudaSuccess) return DCP_ECUDA;
-  if (kept_host_pinned)
-    rc = cuda_ok(cudaMemcpyAsync(kept_host_pinned, &at<Ctrl>(ws, 0)->k, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
   return rc;
 }
 

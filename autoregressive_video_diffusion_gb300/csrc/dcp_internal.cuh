@@ -80,6 +80,7 @@ struct ScanParams {
   uint32_t* bits;          // keep mask as ballot words, one bit per token
   int32_t* status;
   int32_t* kept_dev;
+  int32_t* kept_host;      // page-locked host memory reached through unified addressing (nullable)
   // plane checks (CTAs numbered below n_plane_slices each check 256 planes)
   int32_t update_cache;   // a gather follows: check the receiving planes and the history capacity
   int32_t want_rephase;   // a re-index follows: find the longest history

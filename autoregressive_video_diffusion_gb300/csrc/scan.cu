@@ -332,6 +332,7 @@ __device__ void finalize(const ScanParams& p, int* s_warp, int* s_pick) {
     c->rp_min = (p.want_rephase && all_min_inv > 0 && !bad) ? INT32_MAX - all_min_inv : 0;
     c->abort = abort;
     if (p.kept_dev) *p.kept_dev = k;
+    if (p.kept_host) *reinterpret_cast<volatile int32_t*>(p.kept_host) = k;  // over the host link
     c->acc_len_max1 = 0;
     c->acc_len_min_inv = 0;
     c->acc_first_inv = 0;

@@ -108,7 +108,9 @@ dcp_status dcp_workspace_init(void* workspace_dev, size_t ws_bytes, void* stream
 
 /* Score + threshold + ordered index list for one chunk [how], [differs: prefix pruning uses xref = clean chunk].
  *   x0hat_dev, xref_dev : fp32 [n_tok][d] row-major (the probe-step clean prediction and the final output, or the
- *                         re-noised prediction and the clean observed chunk in the prefix pass).
+ *                         re-noised prediction and the clean observed chunk in the prefix pass).  Device memory, or
+ *                         page-locked host memory (cudaHostAlloc / cudaHostRegister), which the scan kernel then
+ *                         reads directly over the host link; other host memory is refused (DCP_EINVAL).
  *   ell_dev   (nullable): fp32 [n_tok] out, l[n] = (1/d) sum_j (x0hat[n][j] - xref[n][j])^2, fp32 arithmetic.
  *   keep_rule           : 0 keep l > gamma; 1 keep !(l > gamma); 2 the Random ablation of section "premises and
  *                         limits" (Random at the same compression ratio): keep exactly as many tokens as rule 0, the
@@ -153,8 +155,10 @@ dcp_status dcp_rope_reindex(const dcp_cache* cache, const dcp_config* cfg, int32
 /* One full prune step, the unit the library is measured on: score the leaving chunk (x0hat/xref fp32 [C][d]),
  * threshold it, build the index list, re-index the history present before the step from q0_prev to q0, and compact
  * the chunk into the history with its keys re-phased to q0.  Equivalent to dcp_score_mask + dcp_rope_reindex +
- * dcp_compact_layers on the same arguments.  kept_dev (nullable, device) and kept_host_pinned (nullable, pinned
- * host memory, written by a stream-ordered copy) receive the kept count.  dcp_workspace_outputs() gives the device
+ * dcp_compact_layers on the same arguments.  x0hat_dev / xref_dev may be page-locked host memory (as for
+ * dcp_score_mask: read by the scan kernel over the host link, no separate copy).  kept_dev (nullable, device) and
+ * kept_host_pinned (nullable, page-locked host memory, written by the scan kernel's last CTA; valid once the stream
+ * has reached the end of the step) receive the kept count; pageable host memory there is refused (DCP_EINVAL).  dcp_workspace_outputs() gives the device
  * addresses where the step leaves l, the mask and the index list. */
 dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const float* x0hat_dev, const float* xref_dev,
                           int32_t d, int32_t evict_slot, int32_t evict_first_frame, int32_t q0_prev, int32_t q0,

@@ -123,6 +123,33 @@ def test_random_ablation_mid(gpu):
     gpu_vs_oracle_step(MID, hc, ev, keep_rule=2, random_seed=77)
 
 
+@pytest.mark.parametrize("w", [TINY_ROT, MID], ids=["tiny_rotating", "mid"])
+def test_host_resident_score_inputs(gpu, w):
+    """Score rows in page-locked host memory are read by the scan kernel over the host link: the step equals the one
+    on device rows, bit for bit; the kept count lands in page-locked host memory; pageable host memory is refused."""
+    hc, (c, q0_prev, q0) = replay.state_before_last(w)
+    x0, xr = w.score_inputs(c)
+    cfg = devcache.dcp_config(w)
+    a, b = devcache.to_device(hc, w), devcache.to_device(hc, w)
+    ws_a = dcp.new_workspace(dcp.dcp_workspace_size(a, cfg))
+    ws_b = dcp.new_workspace(dcp.dcp_workspace_size(b, cfg))
+    kept_host = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    args = (w.slot_of(c), w.first_frame(c), q0_prev, q0, None)
+    dcp.dcp_prune_step(a, cfg, _cuda(x0), _cuda(xr), *args, None, None, ws_a)
+    dcp.dcp_prune_step(b, cfg, torch.from_numpy(x0).pin_memory(), torch.from_numpy(xr).pin_memory(), *args, None,
+                       kept_host, ws_b)
+    torch.cuda.synchronize()
+    assert dcp.dcp_get_status(b.status) == dcp.DCP_OK
+    ga, gb = devcache.from_device(a, w), devcache.from_device(b, w)
+    assert np.array_equal(ga.k, gb.k) and np.array_equal(ga.v, gb.v)
+    assert np.array_equal(ga.hist_len, gb.hist_len) and np.array_equal(ga.hist_t, gb.hist_t)
+    assert int(kept_host.item()) == int(gb.hist_len.max()) - int(hc.hist_len.max())
+    with pytest.raises(dcp.DcpError):
+        dcp.dcp_prune_step(b, cfg, torch.from_numpy(x0), _cuda(xr), *args, None, None, ws_b)
+    with pytest.raises(dcp.DcpError):
+        dcp.dcp_prune_step(b, cfg, _cuda(x0), _cuda(xr), *args, None, torch.zeros(1, dtype=torch.int32), ws_b)
+
+
 def test_fp32_rows_not_power_of_two(gpu):
     """fp32 keys with D = 36 (144-byte rows, 9 vectors per row) take the general index path."""
     w = scaled(TINY_ROT, D=36, n_temporal_pairs=7, d=10)
