@@ -37,6 +37,8 @@ dcp_status check_cache_cfg(const dcp_cache* c, const dcp_config* g, Derived* d) 
   const int64_t C = (int64_t)g->tokens_per_frame * g->frames_per_chunk;
   if (C > (int64_t(1) << 30)) return DCP_EINVAL;
   if (g->n_temporal_pairs < 0 || g->n_temporal_pairs > c->D / 2) return DCP_EINVAL;
+  // the gather keeps the leaving chunk's cos/sin table (F x n_t entries of 16 bytes) in shared memory
+  if ((int64_t)g->frames_per_chunk * g->n_temporal_pairs * 16 > 100 * 1024) return DCP_EINVAL;
   if (g->pair_layout != 0 || g->rephase_sink != 0) return DCP_EINVAL;
   if (!std::isfinite(g->rope_base) || !(g->rope_base > 0.0)) return DCP_EINVAL;
   if (!std::isfinite(g->g_recent_R) || !std::isfinite(g->g_span_S)) return DCP_EINVAL;
@@ -158,6 +160,7 @@ GatherParams gather_params(const dcp_cache* c, const dcp_config* g, const Derive
   gp.T = g->tokens_per_frame;
   gp.n_t = g->n_temporal_pairs;
   gp.dtype = c->dtype;
+  gp.n_frames = g->frames_per_chunk;
   return gp;
 }
 

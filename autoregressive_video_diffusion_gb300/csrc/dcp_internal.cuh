@@ -144,6 +144,7 @@ struct GatherParams {
   const uint8_t* rot_g;
   int32_t T, n_t, dtype;
   Paging pg;
+  int32_t n_frames;        // F (rows of trig_g)
 };
 
 struct RephaseParams {

@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one full-depth gather launch from the ncu capture summarised in
 # profiles/gather_kernel_full_depth_dram.md.  They describe the kernel sources they were taken on: when the hash of
 # those sources differs, the bench reports no traffic figure.
-GATHER_TRAFFIC_BYTES = 1_502_524_160
-GATHER_TRAFFIC_SOURCES_SHA256 = "7946fea54c372ea1e90cd9e7753813f1c4fc34f72fb40962a66f848ff7daed41"
+GATHER_TRAFFIC_BYTES = 1_502_230_016
+GATHER_TRAFFIC_SOURCES_SHA256 = "29b5f5fadde2d185ceea7817b1e8e46ea87114845d03d6175f2ee8ff6f224ee1"
 
 
 def _gather_traffic():
