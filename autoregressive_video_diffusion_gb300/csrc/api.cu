@@ -161,6 +161,7 @@ GatherParams gather_params(const dcp_cache* c, const dcp_config* g, const Derive
   gp.n_t = g->n_temporal_pairs;
   gp.dtype = c->dtype;
   gp.n_frames = g->frames_per_chunk;
+  gp.no_turn = 0;  // set by the callers that know q0
   return gp;
 }
 
@@ -188,6 +189,16 @@ RephaseParams rephase_params(const dcp_cache* c, const dcp_config* g, const Deri
 }
 
 dcp_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? DCP_OK : DCP_ECUDA; }
+
+// No kept key of the leaving chunk changes phase: g is the identity on every offset q0 - t of the chunk's frames, which
+// holds when the oldest non-sink offset already fits the span (g is then the identity everywhere) or when the chunk's
+// oldest offset is within the recent range R.  Read-time re-index moves keys unturned.  Used only to pick the
+// gather's form (both forms turn whatever the tables say), so it is a speed choice, never a correctness one.
+bool chunk_keeps_phase(const dcp_config* g, const Derived& d, int32_t evict_first_frame, int32_t q0) {
+  if (g->reindex_mode == 1 || g->n_temporal_pairs == 0) return true;
+  const double span_end = g->g_mode == 0 ? g->g_span_S : g->g_recent_R + g->g_span_S;
+  return (double)(q0 - d.T_s) <= span_end || (double)(q0 - evict_first_frame) <= g->g_recent_R;
+}
 
 // ------------------------------------------------------------------------------------------ snapshot helpers
 dcp_status check_live(const dcp_config* g, uint32_t live_slots, int* n_live) {
@@ -475,8 +486,9 @@ dcp_status dcp_compact_layers(const dcp_cache* cache, const dcp_config* cfg, int
   finish_tables(sp);
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
-  return cuda_ok(
-      launch_gather(gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame), st, true, false));
+  GatherParams gp = gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame);
+  gp.no_turn = chunk_keeps_phase(cfg, d, evict_first_frame, q0) ? 1 : 0;
+  return cuda_ok(launch_gather(gp, st, true, false));
 }
 
 dcp_status dcp_rope_reindex(const dcp_cache* cache, const dcp_config* cfg, int32_t q0_prev, int32_t q0, void* ws,
@@ -593,6 +605,7 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
   sp.q0_prev = q0_prev;
   finish_tables(sp);
   GatherParams gp = gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame);
+  gp.no_turn = chunk_keeps_phase(cfg, d, evict_first_frame, q0) ? 1 : 0;
   RephaseParams rp = rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi);
   if (pv) {
     const int64_t per_chunk = d.C / pv->pg.bs;

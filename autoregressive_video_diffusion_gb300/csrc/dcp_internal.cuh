@@ -145,6 +145,7 @@ struct GatherParams {
   int32_t T, n_t, dtype;
   Paging pg;
   int32_t n_frames;        // F (rows of trig_g)
+  int32_t no_turn;         // no kept key changes phase in this step (the phase map is the identity on the chunk)
 };
 
 struct RephaseParams {
@@ -379,6 +380,25 @@ __device__ __forceinline__ void st_stream(void* p, const Vec<8>& v) {
                "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
                : "memory");
 }
+
+// Shared-memory staging (Ampere-style per-thread async copies in, Hopper/Blackwell bulk copies out).
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// Shared -> global bulk copy (TMA engine), tracked by the issuing thread's bulk async-groups.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's generic-proxy writes to shared memory before later async-proxy (bulk copy) reads of it.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // In-place (read-modify-write) accesses of the re-index kernel: plain cached loads and stores, written out as single
 // vector instructions (a struct copy of Vec would be split into 32-bit accesses: one L2 request per word).

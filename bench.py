@@ -869,7 +869,8 @@ def main():
         "us_per_step": res["ms_max"] * 1e3,
         "pct_of_nominal_hbm": 100.0 * (value / world) / NOMINAL_HBM_GBS,
         "pct_of_measured_hbm": 100.0 * (value / world) / peak,
-        "roofline": {"bound": "hbm", "kernel": "gather_kernel", "achieved": gather_gbs, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "gather_staged_kernel" if w is FULL else "gather", "achieved": gather_gbs,
+                     "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": gather_gbs / peak,
                      "traffic": _gather_traffic() if w is FULL else None,
                      "algorithmic_bytes_per_launch": res["gather_bytes"]},
