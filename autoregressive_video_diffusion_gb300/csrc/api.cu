@@ -162,6 +162,7 @@ GatherParams gather_params(const dcp_cache* c, const dcp_config* g, const Derive
   gp.dtype = c->dtype;
   gp.n_frames = g->frames_per_chunk;
   gp.no_turn = 0;  // set by the callers that know q0
+  gp.status = c->status;
   return gp;
 }
 

@@ -146,6 +146,7 @@ struct GatherParams {
   Paging pg;
   int32_t n_frames;        // F (rows of trig_g)
   int32_t no_turn;         // no kept key changes phase in this step (the phase map is the identity on the chunk)
+  int32_t* status;
 };
 
 struct RephaseParams {

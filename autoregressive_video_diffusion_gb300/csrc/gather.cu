@@ -166,9 +166,10 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
 // 16-byte cp.async (the LSU path: fine-grained requests for the scattered source rows, no registers held); when a
 // stage has landed (cp.async groups + one CTA barrier), thread 0 writes the block's two destination runs, which are
 // contiguous, with one bulk copy each (TMA).  Three planes are in flight per CTA, twice what registers allow in the
-// kernel above (measured on the full-depth step: gather 236.0 vs 240.4 us).  Keys whose frame does turn are still
-// turned in shared memory before the store, so the kernel is correct for any step; it is only used when none turns
-// (turning them here measured 279 us against 249 us in the kernel above).
+// kernel above (measured on the full-depth step: gather 236.0 vs 240.4 us).  It moves rows unchanged, so it only
+// serves steps whose phase map is the identity on the leaving chunk (the host decides that from g's closed form);
+// if the tables ever say otherwise it moves nothing and records DCP_EDEVICE.  (Turning keys in shared memory here
+// measured 279 us against 249 us in the kernel above.)
 constexpr int kStagedRows = 64;
 constexpr int kStages = 3;
 
@@ -183,15 +184,12 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
   const int tid = threadIdx.x;
   const int rb = p.row_bytes;
   const int stage_bytes = 2 * R * rb;
-  float4* s_trig = reinterpret_cast<float4*>(smem + S * stage_bytes);
-  int* s_row = reinterpret_cast<int*>(smem + S * stage_bytes + 16 * p.n_frames * p.n_t);  // [0, R): turning frame or
-                                                                                          // -1; [R, 2R): source row
-  for (int e = tid; e < p.n_frames * p.n_t; e += kThreads) s_trig[e] = p.trig_g[e];
+  int* s_row = reinterpret_cast<int*>(smem + S * stage_bytes);  // [0, R): turning frame or -1; [R, 2R): source row
 
   const int64_t common = c->common_len;
   const int first_dyn = c->first_dyn;
   const int nblk = (k + R - 1) / R;
-  int ranges = (int)gridDim.x * 4 / nblk;
+  int ranges = (int)gridDim.x * 2 / nblk;  // longer plane ranges than above: the stages fill once per item
   if (ranges > p.n_planes / 4) ranges = p.n_planes / 4;
   if (ranges < 1) ranges = 1;
   const int ppr = (p.n_planes + ranges - 1) / ranges;
@@ -199,7 +197,6 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
   const int vpr = rb / 16;                  // 16-byte chunks per row
   const int chunks = R * vpr;               // per tensor and stage
   const int per_thread = (2 * chunks + kThreads - 1) / kThreads;
-  const bool bf16 = p.dtype == DCP_BF16;
   const int64_t src0 = p.src_row0 * (int64_t)rb;
 
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
@@ -214,9 +211,10 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
       s_row[R + tid] = s;
       if (first_dyn >= p0 && first_dyn < p1) p.hist_t[common + j0 + tid] = p.evict_first_frame + f;
     }
-    __syncthreads();
-    bool any_turn = false;
-    for (int j = 0; j < nrows; ++j) any_turn |= s_row[j] >= 0;
+    if (__syncthreads_or(tid < nrows && s_row[tid] >= 0)) {
+      if (tid == 0) set_status(p.status, DCP_EDEVICE);  // a key turns: not a step for this form
+      break;
+    }
     const int64_t dst_off = (p.dst_row0 + common + j0) * (int64_t)rb;
     const int nchunks = nrows * vpr;        // per tensor
 
@@ -257,25 +255,7 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
       unsigned char* st = smem + stage * stage_bytes;
       if (tid == 0) bulk_wait_read_all();  // the store issued last iteration has finished reading its stage
       cp_async_wait<S - 2>();              // this thread's copies into stage i have landed
-      if (any_turn) {
-        __syncthreads();                   // every thread's copies are in shared memory
-        for (int e = tid; e < nrows * p.n_t; e += kThreads) {
-          const int row = e / p.n_t, pp = e - row * p.n_t;
-          const int f = s_row[row];
-          if (f < 0) continue;
-          uint32_t* w = reinterpret_cast<uint32_t*>(st + row * rb);
-          float oa, ob;
-          if (bf16) {
-            dev_rotate_bf16in(bf16lo(w[pp]), bf16hi(w[pp]), s_trig[f * p.n_t + pp], oa, ob);
-            w[pp] = pack_bf16x2(oa, ob);
-          } else {
-            dev_rotate(__uint_as_float(w[2 * pp]), __uint_as_float(w[2 * pp + 1]), s_trig[f * p.n_t + pp], oa, ob);
-            w[2 * pp] = __float_as_uint(oa);
-            w[2 * pp + 1] = __float_as_uint(ob);
-          }
-        }
-      }
-      fence_proxy_async_smem();  // the stage's generic-proxy writes before the bulk copy reads them
+      fence_proxy_async_smem();            // the stage's generic-proxy writes before the bulk copy reads them
       __syncthreads();
       if (tid == 0) {
         bulk_store(p.k + pl * p.plane_bytes + dst_off, smem_u32(st), (uint32_t)(nrows * rb));
@@ -299,9 +279,7 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
   if (tid == 0) bulk_wait_all();
 }
 
-size_t staged_smem_bytes(const GatherParams& p) {
-  return (size_t)kStages * 2 * kStagedRows * p.row_bytes + 16 * (size_t)p.n_frames * p.n_t + 8 * kStagedRows;
-}
+size_t staged_smem_bytes(const GatherParams& p) { return (size_t)kStages * 2 * kStagedRows * p.row_bytes + 8 * kStagedRows; }
 
 cudaError_t launch_staged(const GatherParams& p, cudaStream_t s, bool overlap_launch) {
   const size_t smem = staged_smem_bytes(p);
@@ -369,8 +347,11 @@ cudaError_t launch_gather_w(const GatherParams& p, cudaStream_t s, bool overlap_
 }  // namespace
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch, bool paged) {
-  // the staged form when no kept key turns and two CTAs' stages fit in shared memory (bf16 rows up to 256 bytes)
-  if (!paged && p.no_turn && p.row_bytes % 16 == 0 && staged_smem_bytes(p) <= 110 * 1024)
+  // the staged form when no kept key turns, the cache has many planes and two CTAs' stages fit in shared memory (bf16
+  // rows up to 256 bytes).  Measured on the full-depth eviction (1600 planes): step 248.1 vs 250.5 us; on the same
+  // eviction cut to 320 planes the register-staged kernel is faster (step 59.5 vs 64.0 us: items of a few planes
+  // spend much of their time filling and draining three stages).
+  if (!paged && p.no_turn && p.n_planes >= 1024 && p.row_bytes % 16 == 0 && staged_smem_bytes(p) <= 110 * 1024)
     return launch_staged(p, s, overlap_launch);
   if (paged)
     return p.vb == 32 ? launch_gather_w<8, true>(p, s, overlap_launch) : launch_gather_w<4, true>(p, s, overlap_launch);

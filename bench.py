@@ -34,11 +34,11 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-# DRAM bytes (read + write) of one full-depth gather launch from the ncu capture summarised in
+# DRAM bytes (read + write) of one full-depth gather launch (gather_staged_kernel) from the ncu capture summarised in
 # profiles/gather_kernel_full_depth_dram.md.  They describe the kernel sources they were taken on: when the hash of
 # those sources differs, the bench reports no traffic figure.
-GATHER_TRAFFIC_BYTES = 1_502_230_016
-GATHER_TRAFFIC_SOURCES_SHA256 = "29b5f5fadde2d185ceea7817b1e8e46ea87114845d03d6175f2ee8ff6f224ee1"
+GATHER_TRAFFIC_BYTES = 1_504_411_392
+GATHER_TRAFFIC_SOURCES_SHA256 = "be182fd880e1dfd679779e81a995061033167dbc5e62a242a0e04973e8cc9bca"
 
 
 def _gather_traffic():
@@ -329,6 +329,10 @@ def run_gpu(w, steps: int, warmup: int, world: int, rank: int, local: int, clock
     # over the host link (the scan kernel's loads); the kept count comes back to page-locked host memory, written by
     # the scan kernel.  For comparison, the same with explicit copies of the inputs into device buffers first.
     e2e_ms, copy_e2e_ms, h2d_ms = [], [], []
+    if e2e_steps:  # untimed: the first device access to the page-locked inputs sets up their mappings (~0.4 ms)
+        s.restore()
+        s.step(x0=s.x0_host, xr=s.xr_host, kept_host=s.kept_host)
+        torch.cuda.synchronize()
     for _ in range(e2e_steps):
         s.restore()
         s.flush_l2()
@@ -757,6 +761,8 @@ def main():
     ap.add_argument("--oracle-planes", type=int, default=64)
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: the same workload with fewer layers (a few GB on the device)")
+    ap.add_argument("--tokens-per-frame", type=int, default=0,
+                    help="profiling captures only: the same workload with shorter chunks (every plane kept, a few GB)")
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before the timed region")
     ap.add_argument("--case", default="step", choices=["step", "reindex", "score", "random", "read", "snapshot"],
                     help="step: the prune step (default); reindex: dcp_rope_reindex of a 64-plane cache with 90,000 "
@@ -779,6 +785,9 @@ def main():
 
     from synth.workloads import FULL, FULL_ROTATED, scaled
     w = FULL if args.layers <= 0 else scaled(FULL, L=args.layers, name=f"{FULL.name}_L{args.layers}")
+    if args.tokens_per_frame > 0:
+        T = args.tokens_per_frame
+        w = scaled(w, tokens_per_frame=T, hist_cap=4 * T, name=f"{w.name}_T{T}")
     world, rank, local = dist_setup() if args.impl == "dcp" else (int(os.environ.get("WORLD_SIZE", "1")),
                                                                  int(os.environ.get("RANK", "0")), 0)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
