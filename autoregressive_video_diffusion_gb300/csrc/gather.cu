@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
 // measured 279 us against 249 us in the kernel above.)
 constexpr int kStagedRows = 64;
 constexpr int kStages = 3;
+constexpr int kMaxChunksPerThread = 9;  // 2 x 64 rows of up to 288 bytes in 16-byte chunks over 256 threads
 
 __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherParams p) {
   constexpr int S = kStages, R = kStagedRows;
@@ -218,23 +219,37 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
     const int64_t dst_off = (p.dst_row0 + common + j0) * (int64_t)rb;
     const int nchunks = nrows * vpr;        // per tensor
 
+    // this thread's 16-byte chunks of the block: the same (source, stage offset) pairs for every plane of the item
+    int c_src[kMaxChunksPerThread];          // byte offset inside the leaving chunk's rows, -1 when unused
+    uint32_t c_dst[kMaxChunksPerThread];     // byte offset inside a stage (V chunks past the K half)
+    uint32_t c_v = 0;                        // bit u: chunk u is a V chunk
+#pragma unroll
+    for (int u = 0; u < kMaxChunksPerThread; ++u) {
+      const int e = tid + kThreads * u;
+      const int t = e >= chunks;  // tensor: K, then V
+      const int ci = e - t * chunks;
+      c_src[u] = -1;
+      c_dst[u] = 0;
+      if (u < per_thread && ci < nchunks) {
+        const int row = ci / vpr, col = ci - row * vpr;
+        c_src[u] = s_row[R + row] * rb + col * 16;
+        c_dst[u] = (uint32_t)(t * R * rb + row * rb + col * 16);
+        c_v |= (uint32_t)t << u;
+      }
+    }
+
     auto receives = [&](int pl) { return !(p.head_is_static && __ldg(p.head_is_static + pl)); };
     auto next_plane = [&](int pl) {
       while (pl < p1 && !receives(pl)) ++pl;
       return pl;
     };
     auto issue = [&](int stage, int pl) {
-      unsigned char* st = smem + stage * stage_bytes;
-      for (int u = 0; u < per_thread; ++u) {
-        const int e = tid + kThreads * u;
-        const int t = e >= chunks;  // tensor: K, then V
-        const int ci = e - t * chunks;
-        if (ci < nchunks) {
-          const int row = ci / vpr, col = ci - row * vpr;
-          cp_async16(smem_u32(st + t * R * rb + row * rb + col * 16),
-                     (t ? p.v : p.k) + pl * p.plane_bytes + src0 + (int64_t)s_row[R + row] * rb + col * 16);
-        }
-      }
+      const uint32_t st = smem_u32(smem + stage * stage_bytes);
+      const char* kp = p.k + pl * p.plane_bytes + src0;
+      const char* vp = p.v + pl * p.plane_bytes + src0;
+#pragma unroll
+      for (int u = 0; u < kMaxChunksPerThread; ++u)
+        if (c_src[u] >= 0) cp_async16(st + c_dst[u], ((c_v >> u) & 1u ? vp : kp) + c_src[u]);
     };
 
     int load_pl = next_plane(p0);
@@ -351,7 +366,8 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_la
   // rows up to 256 bytes).  Measured on the full-depth eviction (1600 planes): step 248.1 vs 250.5 us; on the same
   // eviction cut to 320 planes the register-staged kernel is faster (step 59.5 vs 64.0 us: items of a few planes
   // spend much of their time filling and draining three stages).
-  if (!paged && p.no_turn && p.n_planes >= 1024 && p.row_bytes % 16 == 0 && staged_smem_bytes(p) <= 110 * 1024)
+  if (!paged && p.no_turn && p.n_planes >= 1024 && p.row_bytes % 16 == 0 && p.row_bytes <= 288 &&
+      staged_smem_bytes(p) <= 110 * 1024)
     return launch_staged(p, s, overlap_launch);
   if (paged)
     return p.vb == 32 ? launch_gather_w<8, true>(p, s, overlap_launch) : launch_gather_w<4, true>(p, s, overlap_launch);
