@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one full-depth gather launch (gather_staged_kernel) from the ncu capture summarised in
 # profiles/gather_kernel_full_depth_dram.md.  They describe the kernel sources they were taken on: when the hash of
 # those sources differs, the bench reports no traffic figure.
-GATHER_TRAFFIC_BYTES = 1_504_411_392
-GATHER_TRAFFIC_SOURCES_SHA256 = "be182fd880e1dfd679779e81a995061033167dbc5e62a242a0e04973e8cc9bca"
+GATHER_TRAFFIC_BYTES = 1_503_610_880
+GATHER_TRAFFIC_SOURCES_SHA256 = "1c8c67b74fedbd394c9931ec4632c335e63f03ed6476349a4230230229a92da0"
 
 
 def _gather_traffic():
