@@ -484,11 +484,13 @@ dcp_status dcp_compact_layers(const dcp_cache* cache, const dcp_config* cfg, int
   sp.g_frames = cfg->frames_per_chunk;
   sp.q0 = q0;
   sp.q0_prev = q0;
+  const bool no_turn = chunk_keeps_phase(cfg, d, evict_first_frame, q0);
+  if (no_turn) sp.g_frames = 0;  // no table for the leaving chunk: its keys move unturned
   finish_tables(sp);
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
   GatherParams gp = gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame);
-  gp.no_turn = chunk_keeps_phase(cfg, d, evict_first_frame, q0) ? 1 : 0;
+  gp.no_turn = no_turn ? 1 : 0;
   return cuda_ok(launch_gather(gp, st, true, false));
 }
 
@@ -604,9 +606,10 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
   sp.h_hi = rephase ? evict_first_frame : d.T_s;
   sp.q0 = q0;
   sp.q0_prev = q0_prev;
-  finish_tables(sp);
   GatherParams gp = gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame);
   gp.no_turn = chunk_keeps_phase(cfg, d, evict_first_frame, q0) ? 1 : 0;
+  if (gp.no_turn) sp.g_frames = 0;  // no table for the leaving chunk: its keys move unturned
+  finish_tables(sp);
   RephaseParams rp = rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi);
   if (pv) {
     const int64_t per_chunk = d.C / pv->pg.bs;

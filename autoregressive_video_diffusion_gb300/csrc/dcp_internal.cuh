@@ -145,7 +145,8 @@ struct GatherParams {
   int32_t T, n_t, dtype;
   Paging pg;
   int32_t n_frames;        // F (rows of trig_g)
-  int32_t no_turn;         // no kept key changes phase in this step (the phase map is the identity on the chunk)
+  int32_t no_turn;         // no kept key changes phase in this step (the phase map is the identity on the chunk):
+                           // the scan builds no trig_g / rot_g for it and the kernels must not read them
   int32_t* status;
 };
 

@@ -22,7 +22,7 @@
 // Bookkeeping folded in: the item holding the first block of a receiving plane sets its hist_len to
 // common_len + k, and the items of the lowest receiving plane append the kept frames to hist_t.
 //
-// A staged form (below) serves the steps in which no kept key turns.
+// A staged form (below) serves the steps in which no kept key turns, on caches of 1024 planes or more.
 //
 // Paged caches (block pools addressed through block tables) use the same decomposition: a thread's source and
 // destination offsets inside a plane come from the tables once per item, and a plane's base from its layer and head.
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
           src_rel[u] = s * p.row_bytes + vec * VB;
           dst_rel[u] = row * p.row_bytes + vec * VB;
         }
-        if (vec < temporal_vecs && __ldg(p.rot_g + f)) rot[u] = (f << 16) | vec;
+        if (vec < temporal_vecs && !p.no_turn && __ldg(p.rot_g + f)) rot[u] = (f << 16) | vec;
         if (vec == 0 && first_dyn >= p0 && first_dyn < p1) p.hist_t[common + j0 + row] = p.evict_first_frame + f;
       }
     }
@@ -167,9 +167,9 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
 // stage has landed (cp.async groups + one CTA barrier), thread 0 writes the block's two destination runs, which are
 // contiguous, with one bulk copy each (TMA).  Three planes are in flight per CTA, twice what registers allow in the
 // kernel above (measured on the full-depth step: gather 236.0 vs 240.4 us).  It moves rows unchanged, so it only
-// serves steps whose phase map is the identity on the leaving chunk (the host decides that from g's closed form);
-// if the tables ever say otherwise it moves nothing and records DCP_EDEVICE.  (Turning keys in shared memory here
-// measured 279 us against 249 us in the kernel above.)
+// serves steps whose phase map is the identity on the leaving chunk (no_turn: decided on the host from g's closed
+// form; the scan then builds no cos/sin table for the chunk).  (Turning keys in shared memory here measured 279 us
+// against 249 us in the kernel above.)
 constexpr int kStagedRows = 64;
 constexpr int kStages = 3;
 constexpr int kMaxChunksPerThread = 9;  // 2 x 64 rows of up to 288 bytes in 16-byte chunks over 256 threads
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
   const int tid = threadIdx.x;
   const int rb = p.row_bytes;
   const int stage_bytes = 2 * R * rb;
-  int* s_row = reinterpret_cast<int*>(smem + S * stage_bytes);  // [0, R): turning frame or -1; [R, 2R): source row
+  int* s_row = reinterpret_cast<int*>(smem + S * stage_bytes);  // [R, 2R): source rows of the block
 
   const int64_t common = c->common_len;
   const int first_dyn = c->first_dyn;
@@ -207,15 +207,10 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
     __syncthreads();  // the previous item's stages and rows are no longer read
     if (tid < nrows) {
       const int s = __ldg(p.idx + j0 + tid);
-      const int f = s / p.T;
-      s_row[tid] = __ldg(p.rot_g + f) ? f : -1;
       s_row[R + tid] = s;
-      if (first_dyn >= p0 && first_dyn < p1) p.hist_t[common + j0 + tid] = p.evict_first_frame + f;
+      if (first_dyn >= p0 && first_dyn < p1) p.hist_t[common + j0 + tid] = p.evict_first_frame + s / p.T;
     }
-    if (__syncthreads_or(tid < nrows && s_row[tid] >= 0)) {
-      if (tid == 0) set_status(p.status, DCP_EDEVICE);  // a key turns: not a step for this form
-      break;
-    }
+    __syncthreads();
     const int64_t dst_off = (p.dst_row0 + common + j0) * (int64_t)rb;
     const int nchunks = nrows * vpr;        // per tensor
 
