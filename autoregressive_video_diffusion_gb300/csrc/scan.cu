@@ -283,6 +283,16 @@ __device__ void finalize(const ScanParams& p, int* s_warp, int* s_pick) {
   Ctrl* c = p.ctrl;
   const int n_words = p.n_tiles > 0 ? (p.n_tok + 31) >> 5 : 0;
   const bool random = p.x0hat && p.keep_rule == 2;
+  // the check accumulators (other CTAs' atomics), read now so their round trip overlaps the ballot words' loads
+  int len1 = 0, min_inv = 0, first_inv = 0, longest = 0, bad = 0, all_min_inv = 0;
+  if (threadIdx.x == 0) {
+    len1 = __ldcg(&c->acc_len_max1);
+    min_inv = __ldcg(&c->acc_len_min_inv);
+    first_inv = __ldcg(&c->acc_first_inv);
+    longest = __ldcg(&c->acc_rp_max);
+    bad = __ldcg(&c->acc_bad);
+    all_min_inv = __ldcg(&c->acc_all_min_inv);
+  }
   Pick pk{0ull, 0, false};
   if (random) pk = random_pick(p, n_words, s_warp, s_pick);
   int k = 0;  // same value in every thread
@@ -304,8 +314,6 @@ __device__ void finalize(const ScanParams& p, int* s_warp, int* s_pick) {
   }
   if (threadIdx.x == 0) {
     int abort = 0;
-    const int len1 = __ldcg(&c->acc_len_max1), min_inv = __ldcg(&c->acc_len_min_inv);
-    const int first_inv = __ldcg(&c->acc_first_inv), longest = __ldcg(&c->acc_rp_max), bad = __ldcg(&c->acc_bad);
     const bool has_dyn = p.update_cache && len1 > 0;
     int common = 0, first = -1;
     if ((p.update_cache || p.want_rephase) && bad) {
@@ -329,7 +337,6 @@ __device__ void finalize(const ScanParams& p, int* s_warp, int* s_pick) {
     c->common_len = common;
     c->first_dyn = first;
     c->rp_max = p.want_rephase ? longest : 0;
-    const int all_min_inv = __ldcg(&c->acc_all_min_inv);
     c->rp_min = (p.want_rephase && all_min_inv > 0 && !bad) ? INT32_MAX - all_min_inv : 0;
     c->abort = abort;
     if (p.kept_dev) *p.kept_dev = k;

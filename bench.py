@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one full-depth gather launch (gather_staged_kernel) from the ncu capture summarised in
 # profiles/gather_kernel_full_depth_dram.md.  They describe the kernel sources they were taken on: when the hash of
 # those sources differs, the bench reports no traffic figure.
-GATHER_TRAFFIC_BYTES = 1_503_610_880
-GATHER_TRAFFIC_SOURCES_SHA256 = "1c8c67b74fedbd394c9931ec4632c335e63f03ed6476349a4230230229a92da0"
+GATHER_TRAFFIC_BYTES = 1_503_741_440
+GATHER_TRAFFIC_SOURCES_SHA256 = "d9ff93eec3b4f80511b4ff26275969291bb5a58e94f8b4d051146ae57a473345"
 
 
 def _gather_traffic():
