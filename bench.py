@@ -50,6 +50,18 @@ def _gather_traffic():
     return GATHER_TRAFFIC_BYTES if h.hexdigest() == GATHER_TRAFFIC_SOURCES_SHA256 else None
 
 
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part", "hardware")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -508,7 +520,20 @@ def run_head_specialised(w, reps: int):
     return out
 
 
-def run_rollout(w, reindex_mode: int = 0):
+DRIFT_PLANES = (0, 1, 77, 160, 319)  # sampled planes of the 320-plane rollout cache for the drift report
+
+
+def _bits_as_ordered(t):
+    """bf16 / fp32 bit patterns as integers whose differences count ulps (torch, on the device)."""
+    import torch
+    if t.dtype == torch.bfloat16:
+        b = t.view(torch.int16).to(torch.int64)
+        return torch.where(b < 0, -(b & 0x7FFF), b)
+    b = t.view(torch.int32).to(torch.int64)
+    return torch.where(b < 0, -(b & 0x7FFFFFFF), b)
+
+
+def run_rollout(w, reindex_mode: int = 0, eager_keys=None):
     """The minute-long rollout: every chunk generated in turn, a prune step after each one that leaves the window;
     per-step times, and the cumulative PR against FullKV kept by the library's host counter.  With read-time
     re-index (reindex_mode 1) the steps re-index nothing, and the read of the final history at the final q0
@@ -561,7 +586,27 @@ def run_rollout(w, reindex_mode: int = 0):
         nbytes = rows * w.D * w.esize * 2
         out["read_history_keys"] = {"rows": rows, "q0": q0_last, "us": rms * 1e3, "bytes": nbytes,
                                     "GB_per_s": nbytes / (rms * 1e-3) / 1e9}
+        if eager_keys is not None:
+            # drift of the eager path: its keys were turned and rounded at every step; the read turns the raw key
+            # once (within 1 ulp of the exact turn), so their difference is the accumulated rounding
+            n = int(r.cache.hist_len[0].item())
+            nt2 = 2 * w.n_temporal_pairs
+            read = out_keys[list(DRIFT_PLANES), :n].float()
+            eager = eager_keys[:, :n].float()
+            ulps = (_bits_as_ordered(out_keys[list(DRIFT_PLANES), :n, :nt2]) -
+                    _bits_as_ordered(eager_keys[:, :n, :nt2])).abs()
+            pair = torch.sqrt(eager[..., 0:nt2:2] ** 2 + eager[..., 1:nt2:2] ** 2).repeat_interleave(2, dim=-1)
+            rel = (read[..., :nt2] - eager[..., :nt2]).abs() / pair.clamp_min(1e-30)
+            out["drift_eager_vs_read_time"] = {
+                "planes": list(DRIFT_PLANES), "rows": n, "steps": len(steps),
+                "entries_differing": int((ulps > 0).sum().item()), "entries": int(ulps.numel()),
+                "max_ulp": int(ulps.max().item()), "max_of_pair_length": float(rel.max().item()),
+                "non_temporal_bitwise": bool(torch.equal(out_keys[list(DRIFT_PLANES), :n, nt2:],
+                                                         eager_keys[:, :n, nt2:]))}
         del out_keys
+    else:
+        out["_final_keys"] = r.cache.k.view(w.n_planes, w.cap, w.D)[list(DRIFT_PLANES), w.sink_rows:
+                                                                    w.sink_rows + w.hist_cap].clone()
     del r
     torch.cuda.empty_cache()
     return out
@@ -858,7 +903,9 @@ def main():
         extra["mid_bf16_single_eviction"] = run_last_eviction(MID, reps=20)
         extra["head_specialised_prefix"] = run_head_specialised(HS_PREFIX, reps=3)
         extra["minute_rollout_gqa8"] = run_rollout(ROLLOUT)
-        extra["minute_rollout_gqa8_read_time_reindex"] = run_rollout(ROLLOUT, reindex_mode=1)
+        eager_keys = extra["minute_rollout_gqa8"].pop("_final_keys")
+        extra["minute_rollout_gqa8_read_time_reindex"] = run_rollout(ROLLOUT, reindex_mode=1, eager_keys=eager_keys)
+        del eager_keys
         from synth.workloads import scaled
         extra["host_snapshot_restore"] = run_snapshot(scaled(FULL, L=8), reps=5)
     if rank != 0:
@@ -904,7 +951,7 @@ def main():
         secs = [sample.step() for _ in range(5)]
         line["cpu_baseline"] = {"value": sample.bytes_per_step() / float(np.mean(secs)) / 1e9, "unit": "GB/s",
                                 "cores": 1, "kind": "oracle", "sample": sample.describe(5),
-                                "host_cores_available": cores}
+                                "host_cores_available": cores, "host_cpu": _cpu_model()}
     print(json.dumps(line))
 
 
