@@ -493,6 +493,61 @@ def run_last_eviction(w, reps: int):
     return out
 
 
+def run_graph_replay(w, reps: int):
+    """The workload's last eviction from an idle GPU, host submission included: the direct call against the same
+    call recorded in a CUDA graph and replayed (the history restored, untimed, between repetitions)."""
+    import torch
+
+    import autoregressive_video_diffusion_gb300 as dcp
+    r = DeviceRollout(w)
+    ev = w.evictions()
+    for c, q0p, q0 in ev[:-1]:
+        r.prepare(c)
+        r.step(c, q0p, q0)
+    c, q0p, q0 = ev[-1]
+    r.prepare(c)
+    H0 = w.sink_rows
+    hl0, ht0 = r.cache.hist_len.clone(), r.cache.hist_t.clone()
+    kh0 = r.cache.k[:, :, H0:H0 + w.hist_cap].clone()
+
+    def restore():
+        r.cache.hist_len.copy_(hl0)
+        r.cache.hist_t.copy_(ht0)
+        r.cache.k[:, :, H0:H0 + w.hist_cap].copy_(kh0)
+
+    restore()
+    r.step(c, q0p, q0)  # the first call sets up the launch attributes outside capture
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    x0, xr = r.inputs[c]
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            dcp.dcp_prune_step(r.cache, r.cfg, x0, xr, w.slot_of(c), w.first_frame(c), q0p, q0, None, r.kept, None,
+                               r.ws, stream=s)
+
+    def timed(fn):
+        out = []
+        for _ in range(reps):
+            restore()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            out.append(a.elapsed_time(b))
+        return float(np.median(out[3:]))
+
+    direct = timed(lambda: r.step(c, q0p, q0))
+    graph = timed(lambda: g.replay())
+    r.check()
+    del g, r
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "direct_us": direct * 1e3, "graph_replay_us": graph * 1e3,
+            "note": "idle GPU before each step, host submission included"}
+
+
 def run_head_specialised(w, reps: int):
     """Prefix pass with 20 static heads per layer: both evictions of the pass, each timed; `reps` passes."""
     import torch
@@ -901,6 +956,7 @@ def main():
         from synth.workloads import HS_PREFIX, MID, ROLLOUT, TINY
         extra["tiny_fp32_single_prune"] = run_last_eviction(TINY, reps=20)
         extra["mid_bf16_single_eviction"] = run_last_eviction(MID, reps=20)
+        extra["cuda_graph_replay"] = [run_graph_replay(TINY, reps=23), run_graph_replay(MID, reps=23)]
         extra["head_specialised_prefix"] = run_head_specialised(HS_PREFIX, reps=3)
         extra["minute_rollout_gqa8"] = run_rollout(ROLLOUT)
         eager_keys = extra["minute_rollout_gqa8"].pop("_final_keys")

@@ -165,6 +165,14 @@ dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const f
                           const uint8_t* head_is_static_dev, int32_t* kept_dev, int32_t* kept_host_pinned,
                           void* workspace_dev, size_t ws_bytes, void* stream);
 
+/* CUDA graphs: dcp_prune_step (and dcp_paged_prune_step, dcp_read_history_keys) enqueue only kernel launches on
+ * `stream` (with programmatic-dependent-launch attributes, which stream capture records as programmatic edges), so a
+ * call can be recorded into a CUDA graph by stream capture and replayed; the replay repeats the step with the
+ * captured arguments and pointers.  Make one call with the same cache geometry outside capture first: the first call
+ * on a device sets up per-kernel launch attributes (shared-memory size, occupancy), which capture does not allow.
+ * Score inputs in page-locked host memory are read at replay time, so a serving loop can refill them between
+ * replays. */
+
 /* Largest workspace dcp_prune_step_noalloc can use: 4 MiB (the full-depth 40 x 40 x 128 cache with 6240-token
  * chunks and max_frames 256 needs about 190 KB). */
 #define DCP_NOALLOC_WORKSPACE_BYTES (4u << 20)

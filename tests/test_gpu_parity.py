@@ -150,6 +150,35 @@ def test_host_resident_score_inputs(gpu, w):
         dcp.dcp_prune_step(b, cfg, _cuda(x0), _cuda(xr), *args, None, torch.zeros(1, dtype=torch.int32), ws_b)
 
 
+@pytest.mark.parametrize("w", [TINY_ROT, MID], ids=["tiny_rotating", "mid"])
+def test_prune_step_in_cuda_graph(gpu, w):
+    """A prune step recorded by stream capture and replayed gives the same cache, bit for bit, as the direct call."""
+    hc, (c, q0_prev, q0) = replay.state_before_last(w)
+    x0, xr = (_cuda(a) for a in w.score_inputs(c))
+    cfg = devcache.dcp_config(w)
+    a, b = devcache.to_device(hc, w), devcache.to_device(hc, w)
+    ws_a = dcp.new_workspace(dcp.dcp_workspace_size(a, cfg))
+    ws_b = dcp.new_workspace(dcp.dcp_workspace_size(b, cfg))
+    args = (w.slot_of(c), w.first_frame(c), q0_prev, q0, None, None, None)
+    dcp.dcp_prune_step(a, cfg, x0, xr, *args, ws_a)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            dcp.dcp_prune_step(b, cfg, x0, xr, *args, ws_b, stream=s)
+    torch.cuda.synchronize()
+    gb0 = devcache.from_device(b, w)
+    assert np.array_equal(gb0.hist_len, hc.hist_len), "capture must not run the step"
+    g.replay()
+    torch.cuda.synchronize()
+    assert dcp.dcp_get_status(b.status) == dcp.DCP_OK
+    ga, gb = devcache.from_device(a, w), devcache.from_device(b, w)
+    assert np.array_equal(ga.k, gb.k) and np.array_equal(ga.v, gb.v)
+    assert np.array_equal(ga.hist_len, gb.hist_len) and np.array_equal(ga.hist_t, gb.hist_t)
+
+
 def test_fp32_rows_not_power_of_two(gpu):
     """fp32 keys with D = 36 (144-byte rows, 9 vectors per row) take the general index path."""
     w = scaled(TINY_ROT, D=36, n_temporal_pairs=7, d=10)
