@@ -222,6 +222,34 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_la
 cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch, bool paged);
 int sm_count();
 
+// Per-device launch set-up of one kernel, made on first use on each device: the dynamic shared-memory opt-in (a
+// per-device function attribute) and the number of CTAs that fit on an SM with that much shared memory.
+constexpr int kMaxDevices = 64;
+struct LaunchCache {
+  size_t opted[kMaxDevices];    // dynamic shared memory opted in so far (bytes)
+  size_t counted[kMaxDevices];  // shared-memory size + 1 that blocks[] was computed for (0: not yet)
+  int blocks[kMaxDevices];
+};
+
+template <typename Kernel>
+cudaError_t launch_setup(LaunchCache& lc, Kernel kernel, int threads, size_t smem, int* blocks_per_sm) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (smem > 48 * 1024 && smem > lc.opted[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    lc.opted[dev] = smem;
+  }
+  if (lc.counted[dev] != smem + 1) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
+    lc.blocks[dev] = n;
+    lc.counted[dev] = smem + 1;
+  }
+  *blocks_per_sm = lc.blocks[dev];
+  return cudaSuccess;
+}
+
 // ------------------------------------------------------------------------------------------ device helpers
 #ifdef __CUDACC__
 

@@ -293,22 +293,10 @@ size_t staged_smem_bytes(const GatherParams& p) { return (size_t)kStages * 2 * k
 
 cudaError_t launch_staged(const GatherParams& p, cudaStream_t s, bool overlap_launch) {
   const size_t smem = staged_smem_bytes(p);
-  static size_t smem_opted = 0;
-  if (smem > smem_opted) {
-    if (cudaFuncSetAttribute(gather_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return cudaErrorInvalidValue;
-    smem_opted = smem;
-  }
-  static int blocks_per_sm = 0;
-  static size_t smem_of_count = ~(size_t)0;
-  if (smem != smem_of_count) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, gather_staged_kernel, kThreads, smem) !=
-            cudaSuccess ||
-        blocks_per_sm < 1)
-      blocks_per_sm = 1;
-    smem_of_count = smem;
-  }
+  static LaunchCache lc;
+  int blocks_per_sm = 1;
+  const cudaError_t e = launch_setup(lc, gather_staged_kernel, kThreads, smem, &blocks_per_sm);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sm_count() * blocks_per_sm));
   cfg.blockDim = dim3(kThreads);
@@ -325,22 +313,10 @@ cudaError_t launch_staged(const GatherParams& p, cudaStream_t s, bool overlap_la
 template <int NW, bool PAGED>
 cudaError_t launch_gather_w(const GatherParams& p, cudaStream_t s, bool overlap_launch) {
   const size_t smem = 16 * (size_t)p.n_frames * p.n_t;
-  static size_t smem_opted = 48 * 1024;  // dynamic shared memory beyond 48 KB needs an opt-in per kernel
-  if (smem > smem_opted) {
-    if (cudaFuncSetAttribute(gather_kernel<NW, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return cudaErrorInvalidValue;
-    smem_opted = smem;
-  }
-  static int blocks_per_sm = 0;
-  static size_t smem_of_count = ~(size_t)0;
-  if (smem != smem_of_count) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, gather_kernel<NW, PAGED>, kThreads, smem) !=
-            cudaSuccess ||
-        blocks_per_sm < 1)
-      blocks_per_sm = 1;
-    smem_of_count = smem;
-  }
+  static LaunchCache lc;
+  int blocks_per_sm = 1;
+  const cudaError_t e = launch_setup(lc, gather_kernel<NW, PAGED>, kThreads, smem, &blocks_per_sm);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sm_count() * blocks_per_sm));
   cfg.blockDim = dim3(kThreads);

@@ -102,13 +102,10 @@ __global__ void __launch_bounds__(kThreads, 3) read_kernel(const ReadParams p) {
 
 template <int NW, bool PAGED>
 cudaError_t launch_read_w(const ReadParams& p, cudaStream_t s) {
-  static int blocks_per_sm = 0;
-  if (!blocks_per_sm) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, read_kernel<NW, PAGED>, kThreads, 0) !=
-            cudaSuccess ||
-        blocks_per_sm < 1)
-      blocks_per_sm = 1;
-  }
+  static LaunchCache lc;
+  int blocks_per_sm = 1;
+  const cudaError_t e = launch_setup(lc, read_kernel<NW, PAGED>, kThreads, 0, &blocks_per_sm);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sm_count() * blocks_per_sm));
   cfg.blockDim = dim3(kThreads);

@@ -101,13 +101,10 @@ __global__ void __launch_bounds__(kThreads, 3) rephase_kernel(const RephaseParam
 
 template <int NW, bool PAGED>
 cudaError_t launch_rephase_w(const RephaseParams& p, cudaStream_t s, bool overlap_launch) {
-  static int blocks_per_sm = 0;
-  if (!blocks_per_sm) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, rephase_kernel<NW, PAGED>, kThreads, 0) !=
-            cudaSuccess ||
-        blocks_per_sm < 1)
-      blocks_per_sm = 1;
-  }
+  static LaunchCache lc;
+  int blocks_per_sm = 1;
+  const cudaError_t e = launch_setup(lc, rephase_kernel<NW, PAGED>, kThreads, 0, &blocks_per_sm);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sm_count() * blocks_per_sm));
   cfg.blockDim = dim3(kThreads);

@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one full-depth gather launch (gather_staged_kernel) from the ncu capture summarised in
 # profiles/gather_kernel_full_depth_dram.md.  They describe the kernel sources they were taken on: when the hash of
 # those sources differs, the bench reports no traffic figure.
-GATHER_TRAFFIC_BYTES = 1_503_741_440
-GATHER_TRAFFIC_SOURCES_SHA256 = "d9ff93eec3b4f80511b4ff26275969291bb5a58e94f8b4d051146ae57a473345"
+GATHER_TRAFFIC_BYTES = 1_504_600_832
+GATHER_TRAFFIC_SOURCES_SHA256 = "640bcf18fd6b2e8fdc9971ade82159236606bcb9a55afdf1ce983505eaef184f"
 
 
 def _gather_traffic():
