@@ -91,6 +91,7 @@ _SIGS = {
                               _vp, _vp, _sz, _vp], _i32),
     "dcp_abi_paged_cache_size": ([], ctypes.c_uint32),
     "dcp_read_history_keys": ([_pc, _pg, _i32, _i32, _i32, _vp, _vp, _sz, _vp], _i32),
+    "dcp_phase_table": ([_pg, _i32, _i32, _i32, _vp, _vp], _i32),
     "dcp_paged_read_history_keys": ([ctypes.POINTER(DcpPagedCacheC), _pg, _i32, _i32, _i32, _vp, _vp, _sz, _vp],
                                     _i32),
     "dcp_snapshot_max_bytes": ([_pc, _pg, ctypes.c_uint32], _sz),
@@ -424,3 +425,11 @@ def dcp_read_history_keys(cache, cfg: Config, q0: int, plane0: int, n_planes: in
     fn = lib.dcp_paged_read_history_keys if isinstance(cache, PagedKVCache) else lib.dcp_read_history_keys
     _check(fn(ctypes.byref(cc), ctypes.byref(gc), q0, plane0, n_planes, _ptr(out), _ptr(ws), ws.numel(),
               _stream(stream)), "dcp_read_history_keys")
+
+
+def dcp_phase_table(cfg: Config, q0: int, frame_lo: int, frame_hi: int, out: torch.Tensor, stream=None) -> None:
+    """cos/sin entries {c_hi, c_lo, s_hi, s_lo} of the turn t -> t~(t; q0) for frames [frame_lo, frame_hi) and every
+    temporal pair, into out (float32 [(frame_hi - frame_lo) * n_t * 4], device)."""
+    gc = cfg.c()
+    _check(lib.dcp_phase_table(ctypes.byref(gc), q0, frame_lo, frame_hi, _ptr(out), _stream(stream)),
+           "dcp_phase_table")

@@ -543,6 +543,25 @@ dcp_status dcp_paged_prune_step(const dcp_paged_cache* cache, const dcp_config* 
 
 uint32_t dcp_abi_paged_cache_size(void) { return (uint32_t)sizeof(dcp_paged_cache); }
 
+dcp_status dcp_phase_table(const dcp_config* g, int32_t q0, int32_t frame_lo, int32_t frame_hi, float* out,
+                           void* stream) {
+  if (!g || !out || !aligned(out, 16)) return DCP_EINVAL;
+  if (g->tokens_per_frame < 1 || g->frames_per_chunk < 1 || g->sink_chunks < 0 || g->window_chunks < 0)
+    return DCP_EINVAL;
+  if (g->n_temporal_pairs < 1 || !std::isfinite(g->rope_base) || !(g->rope_base > 0.0)) return DCP_EINVAL;
+  if (!std::isfinite(g->g_recent_R) || !std::isfinite(g->g_span_S) || (g->g_mode != 0 && g->g_mode != 1))
+    return DCP_EINVAL;
+  if (g->g_recent_R < (double)g->window_chunks * g->frames_per_chunk) return DCP_EINVAL;
+  if ((g->g_mode == 0 && g->g_span_S < g->g_recent_R) || (g->g_mode == 1 && g->g_span_S < 0.0)) return DCP_EINVAL;
+  const int64_t T_s = (int64_t)g->sink_chunks * g->frames_per_chunk;
+  if (T_s > INT32_MAX || frame_lo < T_s || frame_lo > frame_hi || frame_hi > q0) return DCP_EINVAL;
+  const int64_t n = (int64_t)(frame_hi - frame_lo) * g->n_temporal_pairs;
+  if (n > INT32_MAX) return DCP_EINVAL;
+  return cuda_ok(launch_phase_table(reinterpret_cast<float4*>(out), frame_lo, (int32_t)n, g->n_temporal_pairs,
+                                    g->rope_base, g->g_recent_R, g->g_span_S, g->g_mode, (int32_t)T_s, q0,
+                                    (cudaStream_t)stream));
+}
+
 dcp_status dcp_read_history_keys(const dcp_cache* cache, const dcp_config* cfg, int32_t q0, int32_t plane0,
                                  int32_t n_planes, void* out_dev, void* ws, size_t ws_bytes, void* stream) {
   return read_impl(cache, nullptr, cfg, q0, plane0, n_planes, out_dev, ws, ws_bytes, stream);

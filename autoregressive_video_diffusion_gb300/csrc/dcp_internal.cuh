@@ -81,15 +81,15 @@ struct ScanParams {
   int32_t* status;
   int32_t* kept_dev;
   int32_t* kept_host;      // page-locked host memory reached through unified addressing (nullable)
-  // plane checks (CTAs numbered below n_plane_slices each check 256 planes)
+  // plane checks (the check CTAs, after the tile and table CTAs, each check 256 planes)
   int32_t update_cache;   // a gather follows: check the receiving planes and the history capacity
   int32_t want_rephase;   // a re-index follows: find the longest history
   const int32_t* hist_len;
   const uint8_t* head_is_static;
   int32_t n_planes, n_plane_slices;
   int64_t hist_cap;
-  // paged caches: every block-table entry the step will use must name a block of the pools (CTAs numbered below
-  // n_tbl_slices each check 256 entries of tbl_a followed by tbl_b)
+  // paged caches: every block-table entry the step will use must name a block of the pools (the check CTAs each
+  // check 256 entries of tbl_a followed by tbl_b)
   const int32_t* tbl_a;
   const int32_t* tbl_b;
   int32_t n_tbl_a, n_tbl_b, n_tbl_slices;
@@ -216,6 +216,8 @@ struct ReadParams {
 };
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s);
+cudaError_t launch_phase_table(float4* out, int32_t frame_lo, int32_t n_entries, int32_t n_t, double base, double R,
+                               double S, int32_t g_mode, int32_t T_s, int32_t q0, cudaStream_t s);
 cudaError_t launch_read(const ReadParams& p, cudaStream_t s, bool paged);
 cudaError_t launch_snapshot(const SnapParams& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch, bool paged);

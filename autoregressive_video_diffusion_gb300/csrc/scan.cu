@@ -376,7 +376,28 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanParams p) {
   if (s_last) finalize(p, s_warp, s_pick);
 }
 
+// Phase table on its own (dcp_phase_table): one entry per thread, 64-thread CTAs to spread the fp64 work over SMs.
+__global__ void __launch_bounds__(kTableEntries) phase_table_kernel(float4* out, int32_t frame_lo, int32_t n_entries,
+                                                                    int32_t n_t, double base, double R, double S,
+                                                                    int32_t g_mode, int32_t T_s, int32_t q0) {
+  const int e = blockIdx.x * kTableEntries + threadIdx.x;
+  if (e >= n_entries) return;
+  const int f = e / n_t, pp = e - f * n_t;
+  const double t = (double)(frame_lo + f);
+  const double delta = __dsub_rn(dev_phase(t, (double)q0, (double)T_s, R, S, g_mode), t);
+  const double theta = exp2(__dmul_rn(-(double)pp / (double)n_t, log2(base)));
+  out[e] = dev_trig_entry(__dmul_rn(theta, delta));
+}
+
 }  // namespace
+
+cudaError_t launch_phase_table(float4* out, int32_t frame_lo, int32_t n_entries, int32_t n_t, double base, double R,
+                               double S, int32_t g_mode, int32_t T_s, int32_t q0, cudaStream_t s) {
+  if (n_entries <= 0) return cudaSuccess;
+  phase_table_kernel<<<(n_entries + kTableEntries - 1) / kTableEntries, kTableEntries, 0, s>>>(
+      out, frame_lo, n_entries, n_t, base, R, S, g_mode, T_s, q0);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
   const int checks = p.n_plane_slices > p.n_tbl_slices ? p.n_plane_slices : p.n_tbl_slices;

@@ -243,6 +243,18 @@ typedef struct dcp_paged_cache {
 /* Workspace bytes of dcp_paged_prune_step for this cache/config (0 if either is invalid). */
 size_t dcp_paged_workspace_size(const dcp_paged_cache* cache, const dcp_config* cfg);
 
+/* Phase table of read-time re-index [differs], for kernels that fuse the turn into their own reads of K (attention):
+ * for frames t in [frame_lo, frame_hi) and temporal pairs p < n_t, the turn from a key's own phase t to t~(t; q0):
+ *   out_dev[(t - frame_lo) * n_t + p] = {c_hi, c_lo, s_hi, s_lo}  (four floats, 16-byte aligned),
+ * with cos(phi) = c_hi + c_lo and sin(phi) = s_hi + s_lo to about 40 bits, phi = theta_p * (t~(t; q0) - t) and
+ * theta_p = rope_base^(-p / n_t), evaluated in double precision; c_hi and s_hi carry 16 significant bits, so their
+ * products with bf16 values are exact in fp32.  Pair (a, b) turns to (a cos - b sin, a sin + b cos).  Frames that
+ * keep their phase get {1, 0, 0, 0}.  dcp_read_history_keys applies exactly this table.  One stream-ordered launch.
+ * Host errors: DCP_EINVAL (config fields as for dcp_workspace_size; frame_lo < sink frames, frame_hi > q0,
+ * frame_lo > frame_hi, n_temporal_pairs < 1, null or misaligned out_dev). */
+dcp_status dcp_phase_table(const dcp_config* cfg, int32_t q0, int32_t frame_lo, int32_t frame_hi, float* out_dev,
+                           void* stream);
+
 /* dcp_read_history_keys on a paged cache (history rows found through hist_blocks; entries are checked first). */
 dcp_status dcp_paged_read_history_keys(const dcp_paged_cache* cache, const dcp_config* cfg, int32_t q0,
                                        int32_t plane0, int32_t n_planes, void* out_dev, void* workspace_dev,

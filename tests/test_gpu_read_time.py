@@ -152,3 +152,35 @@ def test_read_reports_history_frame_outside_table(gpu):
     assert st == dcp.DCP_EDEVICE
     assert np.all(g[0, 0] == np.int32(0x1357).view(np.float32))
     dcp.dcp_reset_status(dev.status)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_phase_table(gpu, mode):
+    """dcp_phase_table: each entry's hi + lo parts give cos / sin of theta_p (t~(t; q0) - t) (the oracle's pinned phase
+    map and ladder, numpy's cos / sin) to ~2^-38; the hi parts carry at most 16 significant bits; frames that keep their
+    phase get exactly {1, 0, 0, 0}."""
+    w = scaled(TINY, R=2, S=4 if mode == 0 else 3, g_mode=mode)
+    gcfg = devcache.dcp_config(w, reindex_mode=1)
+    T_s = w.sink_chunks * w.frames_per_chunk
+    q0 = 40
+    n_t = w.n_temporal_pairs
+    out = torch.empty((q0 - T_s) * n_t * 4, dtype=torch.float32, device="cuda")
+    dcp.dcp_phase_table(gcfg, q0, T_s, q0, out)
+    tab = out.view(q0 - T_s, n_t, 4).cpu().numpy().astype(np.float64)
+    moved = 0
+    for i, t in enumerate(range(T_s, q0)):
+        tt = oracle.phase(t, q0, T_s, w.R, w.S, mode)
+        for p in range(n_t):
+            phi = oracle.theta(p, n_t, w.rope_base) * (tt - t)
+            c, s = tab[i, p, 0] + tab[i, p, 1], tab[i, p, 2] + tab[i, p, 3]
+            assert abs(c - np.cos(phi)) < 2.0 ** -38 and abs(s - np.sin(phi)) < 2.0 ** -38
+            if tt == t:
+                assert list(tab[i, p]) == [1.0, 0.0, 0.0, 0.0]
+        moved += tt != t
+    hi = out.view(q0 - T_s, n_t, 4)[..., 0::2].contiguous().view(torch.int32).cpu().numpy()
+    assert np.all(hi & 0xFF == 0), "hi parts must carry at most 16 significant bits"
+    assert moved > 0
+    with pytest.raises(dcp.DcpError):
+        dcp.dcp_phase_table(gcfg, q0, T_s, q0 + 1, out)
+    with pytest.raises(dcp.DcpError):
+        dcp.dcp_phase_table(gcfg, q0, T_s - 1, q0, out)
