@@ -23,11 +23,11 @@ TINY_ROT = scaled(TINY, R=2, S=4)
 HND, NHD = dcp.DCP_PAGED_HND, dcp.DCP_PAGED_NHD
 
 
-def paged_vs_oracle_step(w, hc, ev, bs, layout, head_is_static=None, seed=0):
+def paged_vs_oracle_step(w, hc, ev, bs, layout, head_is_static=None, seed=0, reindex_mode=0):
     c, q0_prev, q0 = ev
     x0, xr = w.score_inputs(c)
     dev = devcache.to_device(hc, w)
-    gcfg = devcache.dcp_config(w)
+    gcfg = devcache.dcp_config(w, reindex_mode=reindex_mode)
     pc = PagedCopy(dev, gcfg, bs, layout, seed)
     ws = dcp.new_workspace(dcp.dcp_paged_workspace_size(pc.cache, gcfg))
     kept = torch.full((1,), -1, dtype=torch.int32, device="cuda")
@@ -37,7 +37,9 @@ def paged_vs_oracle_step(w, hc, ev, bs, layout, head_is_static=None, seed=0):
     assert dcp.dcp_get_status(pc.cache.status) == dcp.DCP_OK
     assert pc.free_blocks_untouched(), "free blocks must not be written"
     o = hc.copy()
-    rc, ell, mask, idx = oracle.prune_step(o, replay.cfg_of(w), x0, xr, w.slot_of(c), w.first_frame(c), q0_prev, q0,
+    ocfg = replay.cfg_of(w)
+    ocfg.reindex_mode = reindex_mode
+    rc, ell, mask, idx = oracle.prune_step(o, ocfg, x0, xr, w.slot_of(c), w.first_frame(c), q0_prev, q0,
                                            head_is_static)
     assert rc == oracle.OK
     # the paged workspace has the layout of the contiguous one: its score outputs sit at the same offsets
@@ -62,6 +64,17 @@ def test_paged_head_specialised(gpu):
     hsm = (np.arange(w.L * w.H) % 3 == 1).astype(np.uint8)
     hc, ev = replay.state_before_last(w, head_is_static=hsm)
     paged_vs_oracle_step(w, hc, ev, 16, NHD, head_is_static=hsm, seed=9)
+
+
+@pytest.mark.parametrize("layout", [HND, NHD], ids=["hnd", "nhd"])
+def test_paged_read_time_step(gpu, layout):
+    """Read-time re-index on a paged cache: keys move bitwise and nothing is re-indexed, as in the oracle."""
+    w = MID
+    cfg = replay.cfg_of(w)
+    cfg.reindex_mode = 1
+    hc, ev = replay.state_before_last(w, cfg=cfg)
+    inexact, _ = paged_vs_oracle_step(w, hc, ev, 16, layout, seed=11, reindex_mode=1)
+    assert inexact == 0
 
 
 def test_paged_bad_table_entry_moves_nothing(gpu):
