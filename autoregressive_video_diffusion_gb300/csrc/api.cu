@@ -486,11 +486,13 @@ dcp_status dcp_compact_layers(const dcp_cache* cache, const dcp_config* cfg, int
   sp.q0_prev = q0;
   const bool no_turn = chunk_keeps_phase(cfg, d, evict_first_frame, q0);
   if (no_turn) sp.g_frames = 0;  // no table for the leaving chunk: its keys move unturned
+  if (head_is_static) sp.dyn_list = at<int32_t>(ws, d.lay.dyn);  // the scan lists the receiving planes
   finish_tables(sp);
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
   GatherParams gp = gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame);
   gp.no_turn = no_turn ? 1 : 0;
+  if (head_is_static) gp.dyn_list = at<int32_t>(ws, d.lay.dyn);
   return cuda_ok(launch_gather(gp, st, true, false));
 }
 
@@ -628,6 +630,10 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
   GatherParams gp = gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame);
   gp.no_turn = chunk_keeps_phase(cfg, d, evict_first_frame, q0) ? 1 : 0;
   if (gp.no_turn) sp.g_frames = 0;  // no table for the leaving chunk: its keys move unturned
+  if (head_is_static) {  // the scan lists the receiving planes; the gather splits that list only
+    sp.dyn_list = at<int32_t>(ws, d.lay.dyn);
+    gp.dyn_list = sp.dyn_list;
+  }
   finish_tables(sp);
   RephaseParams rp = rephase_params(cache, cfg, d, ws, sp.h_lo, sp.h_hi);
   if (pv) {

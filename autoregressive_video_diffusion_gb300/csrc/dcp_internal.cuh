@@ -33,14 +33,16 @@ struct Ctrl {
   int32_t acc_bad;          // some plane's hist_len is outside [0, hist_cap]
   int32_t acc_all_min_inv;  // max over all planes of INT32_MAX - hist_len
   int32_t rp_min;           // shortest history of any plane before the step (rows below it exist in every plane)
+  int32_t acc_n_dyn;        // receiving planes listed so far (head-specialised steps)
+  int32_t n_dyn;            // receiving planes in the list
   int64_t snap_rows;        // snapshot / restore: saved rows per tensor
   int64_t snap_data_off;    // snapshot / restore: byte offset of the K block in the image
-  int32_t pad[44];
+  int32_t pad[42];
 };
 static_assert(sizeof(Ctrl) == 256, "ctrl block is one 256-byte line");
 
 struct Layout {           // byte offsets inside the workspace
-  size_t bits, ell, mask, idx, trig_g, rot_g, trig_h, rot_h, plane_off, total;
+  size_t bits, ell, mask, idx, trig_g, rot_g, trig_h, rot_h, plane_off, dyn, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -57,6 +59,7 @@ inline Layout make_layout(int64_t n_tok, int64_t n_planes, int64_t F, int64_t n_
   L.trig_h = off;     off = align256(off + 16 * (size_t)(max_frames * n_t));
   L.rot_h = off;      off = align256(off + (size_t)max_frames);
   L.plane_off = off;  off = align256(off + 8 * (size_t)(n_planes > 0 ? n_planes + 1 : 0));
+  L.dyn = off;        off = align256(off + 4 * (size_t)(n_planes > 0 ? n_planes : 0));
   L.total = off;
   return L;
 }
@@ -86,6 +89,7 @@ struct ScanParams {
   int32_t want_rephase;   // a re-index follows: find the longest history
   const int32_t* hist_len;
   const uint8_t* head_is_static;
+  int32_t* dyn_list;       // head-specialised steps: the receiving planes are listed here (order not significant)
   int32_t n_planes, n_plane_slices;
   int64_t hist_cap;
   // paged caches: every block-table entry the step will use must name a block of the pools (the check CTAs each
@@ -148,6 +152,8 @@ struct GatherParams {
   int32_t no_turn;         // no kept key changes phase in this step (the phase map is the identity on the chunk):
                            // the scan builds no trig_g / rot_g for it and the kernels must not read them
   int32_t* status;
+  const int32_t* dyn_list; // head-specialised steps: the scan's list of receiving planes (ctrl->n_dyn of them);
+                           // the planes split into ranges along it, so static planes take no share of the work
 };
 
 struct RephaseParams {

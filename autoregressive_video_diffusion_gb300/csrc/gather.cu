@@ -62,10 +62,11 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
   const int nblk = (k + rows_per_item - 1) / rows_per_item;
   // about four smaller items per CTA rather than one large one (measured on the full-depth step: gather 238.9 vs
   // 240.3 us, and 252.2 vs 256.9 us when every key turns)
+  const int n_seq = p.dyn_list ? c->n_dyn : p.n_planes;  // planes split into ranges (all, or the receiving list)
   int ranges = (int)gridDim.x * 4 / nblk;
-  if (ranges > p.n_planes / 4) ranges = p.n_planes / 4;  // at least four planes per item (small caches)
+  if (ranges > n_seq / 4) ranges = n_seq / 4;  // at least four planes per item (small caches)
   if (ranges < 1) ranges = 1;
-  const int ppr = (p.n_planes + ranges - 1) / ranges;
+  const int ppr = (n_seq + ranges - 1) / ranges;
   const int items = nblk * ranges;
   const int ppv = p.dtype == DCP_BF16 ? VB / 4 : VB / 8;   // rotary pairs per vector
   const int temporal_vecs = (p.n_t + ppv - 1) / ppv;
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
 
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int jb = it % nblk, r = it / nblk;
-    const int p0 = r * ppr, p1 = min(p.n_planes, p0 + ppr);
+    const int p0 = r * ppr, p1 = min(n_seq, p0 + ppr);  // positions in the plane sequence
     const int j0 = jb * rows_per_item, nrows = min(rows_per_item, k - j0);
     const int64_t dst_block = PAGED ? 0 : (p.dst_row0 + common + j0) * (int64_t)p.row_bytes;
 
@@ -106,17 +107,20 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
           dst_rel[u] = row * p.row_bytes + vec * VB;
         }
         if (vec < temporal_vecs && !p.no_turn && __ldg(p.rot_g + f)) rot[u] = (f << 16) | vec;
-        if (vec == 0 && first_dyn >= p0 && first_dyn < p1) p.hist_t[common + j0 + row] = p.evict_first_frame + f;
+        const bool writes_t = p.dyn_list ? r == 0 : first_dyn >= p0 && first_dyn < p1;  // one item per row block
+        if (vec == 0 && writes_t) p.hist_t[common + j0 + row] = p.evict_first_frame + f;
       }
     }
 
     // software pipeline over the planes: the next receiving plane's loads are in flight while this one is turned
     // and stored
-    auto receives = [&](int pl) { return !(p.head_is_static && __ldg(p.head_is_static + pl)); };
-    int pl = p0;
-    while (pl < p1 && !receives(pl)) ++pl;
+    auto receives = [&](int j) { return p.dyn_list || !(p.head_is_static && __ldg(p.head_is_static + j)); };
+    auto plane_of = [&](int j) { return p.dyn_list ? __ldg(p.dyn_list + j) : j; };
+    int pj = p0;
+    while (pj < p1 && !receives(pj)) ++pj;
     Vec<NW> ck[SLOTS], cv[SLOTS], nk[SLOTS], nv[SLOTS];
-    if (pl < p1) {
+    if (pj < p1) {
+      const int pl = plane_of(pj);
 #pragma unroll
       for (int u = 0; u < SLOTS; ++u)
         if (src_rel[u] >= 0) {
@@ -124,10 +128,12 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
           ld_stream(cv[u], p.v + plane_base(pl) + src_slot + src_rel[u]);
         }
     }
-    while (pl < p1) {
-      int nx = pl + 1;
-      while (nx < p1 && !receives(nx)) ++nx;
-      if (nx < p1) {
+    while (pj < p1) {
+      const int pl = plane_of(pj);
+      int nj = pj + 1;
+      while (nj < p1 && !receives(nj)) ++nj;
+      if (nj < p1) {
+        const int nx = plane_of(nj);
 #pragma unroll
         for (int u = 0; u < SLOTS; ++u)
           if (src_rel[u] >= 0) {
@@ -154,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
         ck[u] = nk[u];
         cv[u] = nv[u];
       }
-      pl = nx;
+      pj = nj;
     }
   }
 }
@@ -190,10 +196,11 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
   const int64_t common = c->common_len;
   const int first_dyn = c->first_dyn;
   const int nblk = (k + R - 1) / R;
+  const int n_seq = p.dyn_list ? c->n_dyn : p.n_planes;  // planes split into ranges (all, or the receiving list)
   int ranges = (int)gridDim.x * 2 / nblk;  // longer plane ranges than above: the stages fill once per item
-  if (ranges > p.n_planes / 4) ranges = p.n_planes / 4;
+  if (ranges > n_seq / 4) ranges = n_seq / 4;
   if (ranges < 1) ranges = 1;
-  const int ppr = (p.n_planes + ranges - 1) / ranges;
+  const int ppr = (n_seq + ranges - 1) / ranges;
   const int items = nblk * ranges;
   const int vpr = rb / 16;                  // 16-byte chunks per row
   const int chunks = R * vpr;               // per tensor and stage
@@ -202,13 +209,14 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
 
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int jb = it % nblk, r = it / nblk;
-    const int p0 = r * ppr, p1 = min(p.n_planes, p0 + ppr);
+    const int p0 = r * ppr, p1 = min(n_seq, p0 + ppr);  // positions in the plane sequence
     const int j0 = jb * R, nrows = min(R, k - j0);
     __syncthreads();  // the previous item's stages and rows are no longer read
     if (tid < nrows) {
       const int s = __ldg(p.idx + j0 + tid);
       s_row[R + tid] = s;
-      if (first_dyn >= p0 && first_dyn < p1) p.hist_t[common + j0 + tid] = p.evict_first_frame + s / p.T;
+      const bool writes_t = p.dyn_list ? r == 0 : first_dyn >= p0 && first_dyn < p1;  // one item per row block
+      if (writes_t) p.hist_t[common + j0 + tid] = p.evict_first_frame + s / p.T;
     }
     __syncthreads();
     const int64_t dst_off = (p.dst_row0 + common + j0) * (int64_t)rb;
@@ -233,10 +241,11 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
       }
     }
 
-    auto receives = [&](int pl) { return !(p.head_is_static && __ldg(p.head_is_static + pl)); };
-    auto next_plane = [&](int pl) {
-      while (pl < p1 && !receives(pl)) ++pl;
-      return pl;
+    auto receives = [&](int j) { return p.dyn_list || !(p.head_is_static && __ldg(p.head_is_static + j)); };
+    auto plane_of = [&](int j) { return p.dyn_list ? __ldg(p.dyn_list + j) : j; };
+    auto next_plane = [&](int j) {  // next receiving position
+      while (j < p1 && !receives(j)) ++j;
+      return j;
     };
     auto issue = [&](int stage, int pl) {
       const uint32_t st = smem_u32(smem + stage * stage_bytes);
@@ -247,15 +256,15 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
         if (c_src[u] >= 0) cp_async16(st + c_dst[u], ((c_v >> u) & 1u ? vp : kp) + c_src[u]);
     };
 
-    int load_pl = next_plane(p0);
-    int queue[S];
+    int load_j = next_plane(p0);
+    int queue[S];  // the plane each stage holds
     int n_issued = 0;
     for (int q = 0; q < S - 1; ++q) {
-      if (load_pl < p1) {
-        issue(q, load_pl);
-        queue[q] = load_pl;
+      if (load_j < p1) {
+        queue[q] = plane_of(load_j);
+        issue(q, queue[q]);
         ++n_issued;
-        load_pl = next_plane(load_pl + 1);
+        load_j = next_plane(load_j + 1);
       }
       cp_async_commit();  // one group per slot, empty or not, so the group count stays uniform
     }
@@ -274,12 +283,12 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
         if (jb == 0) p.hist_len[pl] = (int32_t)(common + k);
       }
       // refill the stage the previous store read (thread 0 waited for that store before the barrier above)
-      if (load_pl < p1) {
+      if (load_j < p1) {
         const int rs = (i + S - 1) % S;
-        issue(rs, load_pl);
-        queue[rs] = load_pl;
+        queue[rs] = plane_of(load_j);
+        issue(rs, queue[rs]);
         ++n_issued;
-        load_pl = next_plane(load_pl + 1);
+        load_j = next_plane(load_j + 1);
       }
       cp_async_commit();
     }

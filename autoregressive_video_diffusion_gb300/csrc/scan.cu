@@ -122,7 +122,7 @@ __device__ void tile_work(const ScanParams& p, int tile_id, float* s_ell) {
   if ((tid & 31) == 0 && w * 32 < ntok) p.bits[(t0 >> 5) + w] = word;
 }
 
-__device__ void plane_checks(const ScanParams& p, int slice) {
+__device__ void plane_checks(const ScanParams& p, int slice, int* s_warp, int* s_base) {
   const int pl = slice * kThreads + threadIdx.x;
   int len1 = 0, min_inv = 0, first_inv = 0, longest = 0, bad = 0, all_min_inv = 0;
   if (pl < p.n_planes) {
@@ -139,6 +139,13 @@ __device__ void plane_checks(const ScanParams& p, int slice) {
         first_inv = INT32_MAX - pl;
       }
     }
+  }
+  if (p.dyn_list) {  // list the receiving planes: in plane order within this CTA's 256, one atomic per CTA
+    int total = 0;
+    const int rank = block_exclusive_scan(len1 > 0 ? 1 : 0, s_warp, &total);
+    if (threadIdx.x == 0) *s_base = total ? atomicAdd(&p.ctrl->acc_n_dyn, total) : 0;
+    __syncthreads();
+    if (len1 > 0) p.dyn_list[*s_base + rank] = pl;
   }
   len1 = __reduce_max_sync(kFull, len1);
   min_inv = __reduce_max_sync(kFull, min_inv);
@@ -284,8 +291,9 @@ __device__ void finalize(const ScanParams& p, int* s_warp, int* s_pick) {
   const int n_words = p.n_tiles > 0 ? (p.n_tok + 31) >> 5 : 0;
   const bool random = p.x0hat && p.keep_rule == 2;
   // the check accumulators (other CTAs' atomics), read now so their round trip overlaps the ballot words' loads
-  int len1 = 0, min_inv = 0, first_inv = 0, longest = 0, bad = 0, all_min_inv = 0;
+  int len1 = 0, min_inv = 0, first_inv = 0, longest = 0, bad = 0, all_min_inv = 0, n_dyn = 0;
   if (threadIdx.x == 0) {
+    n_dyn = __ldcg(&c->acc_n_dyn);
     len1 = __ldcg(&c->acc_len_max1);
     min_inv = __ldcg(&c->acc_len_min_inv);
     first_inv = __ldcg(&c->acc_first_inv);
@@ -347,6 +355,8 @@ __device__ void finalize(const ScanParams& p, int* s_warp, int* s_pick) {
     c->acc_rp_max = 0;
     c->acc_all_min_inv = 0;
     c->acc_bad = 0;
+    c->n_dyn = n_dyn;
+    c->acc_n_dyn = 0;
     c->done = 0u;
   }
 }
@@ -361,7 +371,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanParams p) {
   const int check0 = p.n_tiles + p.n_trig_blocks;  // the check CTAs follow the tile and table CTAs
   if (id < p.n_tiles) tile_work(p, id, s_ell);
   else if (id < check0) table_work(p, id - p.n_tiles);
-  if (id >= check0 && id - check0 < p.n_plane_slices) plane_checks(p, id - check0);
+  if (id >= check0 && id - check0 < p.n_plane_slices) plane_checks(p, id - check0, s_warp, &s_last);
   if (id >= check0 && id - check0 < p.n_tbl_slices) table_checks(p, id - check0);
 
   // Completion: the final CTA reads the ballot words (stored by lane 0 of each tile warp) and the atomically folded
