@@ -38,7 +38,7 @@ namespace {
 // next plane's loads in flight while the current plane is turned and stored (measured on the full-depth step:
 // 248.5 us vs 253.2 us without the pipeline at 3 CTAs/SM; 259.2 us vs 269.9 us when every key turns; at 3 CTAs/SM
 // the pipelined form spills).
-template <int NW, bool PAGED>
+template <int NW, bool PAGED, bool LIST>
 __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams p) {
   using Off = typename std::conditional<PAGED, int64_t, int>::type;
   constexpr int VB = NW * 4;                      // bytes per vector
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
   const int nblk = (k + rows_per_item - 1) / rows_per_item;
   // about four smaller items per CTA rather than one large one (measured on the full-depth step: gather 238.9 vs
   // 240.3 us, and 252.2 vs 256.9 us when every key turns)
-  const int n_seq = p.dyn_list ? c->n_dyn : p.n_planes;  // planes split into ranges (all, or the receiving list)
+  const int n_seq = LIST ? c->n_dyn : p.n_planes;  // planes split into ranges (all, or the receiving list)
   int ranges = (int)gridDim.x * 4 / nblk;
   if (ranges > n_seq / 4) ranges = n_seq / 4;  // at least four planes per item (small caches)
   if (ranges < 1) ranges = 1;
@@ -107,15 +107,15 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
           dst_rel[u] = row * p.row_bytes + vec * VB;
         }
         if (vec < temporal_vecs && !p.no_turn && __ldg(p.rot_g + f)) rot[u] = (f << 16) | vec;
-        const bool writes_t = p.dyn_list ? r == 0 : first_dyn >= p0 && first_dyn < p1;  // one item per row block
+        const bool writes_t = LIST ? r == 0 : first_dyn >= p0 && first_dyn < p1;  // one item per row block
         if (vec == 0 && writes_t) p.hist_t[common + j0 + row] = p.evict_first_frame + f;
       }
     }
 
     // software pipeline over the planes: the next receiving plane's loads are in flight while this one is turned
     // and stored
-    auto receives = [&](int j) { return p.dyn_list || !(p.head_is_static && __ldg(p.head_is_static + j)); };
-    auto plane_of = [&](int j) { return p.dyn_list ? __ldg(p.dyn_list + j) : j; };
+    auto receives = [&](int j) { return LIST || !(p.head_is_static && __ldg(p.head_is_static + j)); };
+    auto plane_of = [&](int j) { return LIST ? __ldg(p.dyn_list + j) : j; };
     int pj = p0;
     while (pj < p1 && !receives(pj)) ++pj;
     Vec<NW> ck[SLOTS], cv[SLOTS], nk[SLOTS], nv[SLOTS];
@@ -319,12 +319,12 @@ cudaError_t launch_staged(const GatherParams& p, cudaStream_t s, bool overlap_la
   return cudaLaunchKernelEx(&cfg, gather_staged_kernel, p);
 }
 
-template <int NW, bool PAGED>
+template <int NW, bool PAGED, bool LIST>
 cudaError_t launch_gather_w(const GatherParams& p, cudaStream_t s, bool overlap_launch) {
   const size_t smem = 16 * (size_t)p.n_frames * p.n_t;
   static LaunchCache lc;
   int blocks_per_sm = 1;
-  const cudaError_t e = launch_setup(lc, gather_kernel<NW, PAGED>, kThreads, smem, &blocks_per_sm);
+  const cudaError_t e = launch_setup(lc, gather_kernel<NW, PAGED, LIST>, kThreads, smem, &blocks_per_sm);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sm_count() * blocks_per_sm));
@@ -336,7 +336,7 @@ cudaError_t launch_gather_w(const GatherParams& p, cudaStream_t s, bool overlap_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_launch ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gather_kernel<NW, PAGED>, p);
+  return cudaLaunchKernelEx(&cfg, gather_kernel<NW, PAGED, LIST>, p);
 }
 
 }  // namespace
@@ -349,9 +349,20 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_la
   if (!paged && p.no_turn && p.n_planes >= 1024 && p.row_bytes % 16 == 0 && p.row_bytes <= 288 &&
       staged_smem_bytes(p) <= 110 * 1024)
     return launch_staged(p, s, overlap_launch);
+  // the receiving-plane list (head-specialised steps) is a compile-time choice: reading the plane sequence through
+  // it in every step cost the paged full-depth gather 243 -> 264 us
+  if (p.dyn_list) {
+    if (paged)
+      return p.vb == 32 ? launch_gather_w<8, true, true>(p, s, overlap_launch)
+                        : launch_gather_w<4, true, true>(p, s, overlap_launch);
+    return p.vb == 32 ? launch_gather_w<8, false, true>(p, s, overlap_launch)
+                      : launch_gather_w<4, false, true>(p, s, overlap_launch);
+  }
   if (paged)
-    return p.vb == 32 ? launch_gather_w<8, true>(p, s, overlap_launch) : launch_gather_w<4, true>(p, s, overlap_launch);
-  return p.vb == 32 ? launch_gather_w<8, false>(p, s, overlap_launch) : launch_gather_w<4, false>(p, s, overlap_launch);
+    return p.vb == 32 ? launch_gather_w<8, true, false>(p, s, overlap_launch)
+                      : launch_gather_w<4, true, false>(p, s, overlap_launch);
+  return p.vb == 32 ? launch_gather_w<8, false, false>(p, s, overlap_launch)
+                    : launch_gather_w<4, false, false>(p, s, overlap_launch);
 }
 
 }  // namespace dcp

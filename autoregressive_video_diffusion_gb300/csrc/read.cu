@@ -6,7 +6,8 @@
 // moves, the keys stay at the phase t they were generated with and each read turns them once, from t to
 // t~(t; q0), so nothing accumulates rounding from one step to the next.
 //
-// Plane streaming as in the other kernels: an item is (block of history rows, range of planes); each thread owns one
+// Plane streaming as in the other kernels: an item is (block of history rows, range of planes), each CTA taking one
+// contiguous, equal share of all (block, plane) pairs; each thread owns one
 // (row, vector) of the block, so a warp reads whole rows; the vectors that hold temporal pairs load their cos/sin
 // entries (which depend only on the row's frame) into registers once per item.  Four planes in flight per thread.
 // Rows past a plane's own history length are skipped.  The phase table comes from the scan kernel's table CTAs,
@@ -34,11 +35,9 @@ __global__ void __launch_bounds__(kThreads, 3) read_kernel(const ReadParams p) {
   const int ppv = p.dtype == DCP_BF16 ? VB / 4 : VB / 8;
   const int rows_per_item = kThreads / p.vpr;  // vpr <= kThreads: rows are at most 4 KiB
   const int nblk = (rp_max + rows_per_item - 1) / rows_per_item;
-  int ranges = (int)gridDim.x / nblk;
-  if (ranges < 1) ranges = 1;
-  if (ranges > p.n_planes) ranges = p.n_planes;
-  const int ppr = (p.n_planes + ranges - 1) / ranges;
-  const int items = nblk * ranges;
+  // One contiguous, equal share of the (row block, plane) units per CTA, block-major.
+  const int64_t units = (int64_t)nblk * p.n_planes;
+  const int64_t u_end = units * (blockIdx.x + 1) / gridDim.x;
   const int row_in_item = threadIdx.x / p.vpr, vec = threadIdx.x - row_in_item * p.vpr;
   const int64_t hist0 = PAGED ? 0 : p.hist_row0 * (int64_t)p.row_bytes;
   const int64_t out_plane = p.hist_cap * (int64_t)p.row_bytes;
@@ -47,9 +46,11 @@ __global__ void __launch_bounds__(kThreads, 3) read_kernel(const ReadParams p) {
     return (int64_t)pl * p.plane_bytes;
   };
 
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    const int jb = it % nblk, r = it / nblk;
-    const int p0 = r * ppr, p1 = min(p.n_planes, p0 + ppr);
+  for (int64_t u = units * blockIdx.x / gridDim.x; u < u_end;) {
+    const int jb = (int)(u / p.n_planes);
+    const int p0 = (int)(u - (int64_t)jb * p.n_planes);
+    const int p1 = (int)min((int64_t)p.n_planes, u_end - (int64_t)jb * p.n_planes);
+    u = (int64_t)jb * p.n_planes + p1;
     const int row = jb * rows_per_item + row_in_item;
 
     bool valid = row_in_item < rows_per_item && row < rp_max;

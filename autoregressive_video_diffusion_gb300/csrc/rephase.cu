@@ -8,7 +8,8 @@
 //
 // Only the vectors of a row that hold temporal pairs are read and written (for bf16, D = 128 and n_t = 22 that is
 // the first 96 bytes of each 256-byte row: three 32-byte vectors); values and the other key dims are never touched.
-// Plane streaming as in the gather: an item is (block of history rows, range of planes).  Each thread owns one
+// Plane streaming as in the gather: an item is (block of history rows, range of planes), and each CTA takes one
+// contiguous, equal share of all (block, plane) pairs.  Each thread owns one
 // (row, vector) of the block; the cos/sin entries of that vector's pairs depend only on the row's frame, so they are
 // loaded into registers once per item and reused for every plane.  Planes are taken four at a time, so four
 // independent loads are in flight per thread.  Rows whose frame does not move, and rows past a plane's own history
@@ -37,11 +38,10 @@ __global__ void __launch_bounds__(kThreads, 3) rephase_kernel(const RephaseParam
   const int ppv = p.dtype == DCP_BF16 ? VB / 4 : VB / 8;
   const int rows_per_item = kThreads / p.nvt;  // nvt <= kThreads: rows are at most 4 KiB
   const int nblk = (rp_max + rows_per_item - 1) / rows_per_item;
-  int ranges = (int)gridDim.x / nblk;
-  if (ranges < 1) ranges = 1;
-  if (ranges > p.n_planes) ranges = p.n_planes;
-  const int ppr = (p.n_planes + ranges - 1) / ranges;
-  const int items = nblk * ranges;
+  // Each CTA takes one contiguous share of the (row block, plane) units, block-major, so every CTA gets the same
+  // number of planes give or take one: whole items dealt round-robin left a third of the CTAs a third item.
+  const int64_t units = (int64_t)nblk * p.n_planes;
+  const int64_t u_end = units * (blockIdx.x + 1) / gridDim.x;
   const int row_in_item = threadIdx.x / p.nvt, vec = threadIdx.x - row_in_item * p.nvt;
   const int64_t hist0 = PAGED ? 0 : p.hist_row0 * (int64_t)p.row_bytes;
   auto plane_base = [&](int pl) -> int64_t {
@@ -49,9 +49,11 @@ __global__ void __launch_bounds__(kThreads, 3) rephase_kernel(const RephaseParam
     return (int64_t)pl * p.plane_bytes;
   };
 
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    const int jb = it % nblk, r = it / nblk;
-    const int p0 = r * ppr, p1 = min(p.n_planes, p0 + ppr);
+  for (int64_t u = units * blockIdx.x / gridDim.x; u < u_end;) {
+    const int jb = (int)(u / p.n_planes);
+    const int p0 = (int)(u - (int64_t)jb * p.n_planes);
+    const int p1 = (int)min((int64_t)p.n_planes, u_end - (int64_t)jb * p.n_planes);
+    u = (int64_t)jb * p.n_planes + p1;
     const int row = jb * rows_per_item + row_in_item;
 
     bool live = false;
