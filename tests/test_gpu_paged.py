@@ -23,11 +23,11 @@ TINY_ROT = scaled(TINY, R=2, S=4)
 HND, NHD = dcp.DCP_PAGED_HND, dcp.DCP_PAGED_NHD
 
 
-def paged_vs_oracle_step(w, hc, ev, bs, layout, head_is_static=None, seed=0, reindex_mode=0):
+def paged_vs_oracle_step(w, hc, ev, bs, layout, head_is_static=None, seed=0, **cfg_over):
     c, q0_prev, q0 = ev
     x0, xr = w.score_inputs(c)
     dev = devcache.to_device(hc, w)
-    gcfg = devcache.dcp_config(w, reindex_mode=reindex_mode)
+    gcfg = devcache.dcp_config(w, **cfg_over)
     pc = PagedCopy(dev, gcfg, bs, layout, seed)
     ws = dcp.new_workspace(dcp.dcp_paged_workspace_size(pc.cache, gcfg))
     kept = torch.full((1,), -1, dtype=torch.int32, device="cuda")
@@ -38,7 +38,8 @@ def paged_vs_oracle_step(w, hc, ev, bs, layout, head_is_static=None, seed=0, rei
     assert pc.free_blocks_untouched(), "free blocks must not be written"
     o = hc.copy()
     ocfg = replay.cfg_of(w)
-    ocfg.reindex_mode = reindex_mode
+    for key, val in cfg_over.items():
+        setattr(ocfg, key, val)
     rc, ell, mask, idx = oracle.prune_step(o, ocfg, x0, xr, w.slot_of(c), w.first_frame(c), q0_prev, q0,
                                            head_is_static)
     assert rc == oracle.OK

@@ -1,0 +1,100 @@
+"""Seeded sweep of small geometries: every eviction of each drawn workload runs on the GPU and in the oracle from the
+same host state, with the bars of test_gpu_parity.py (masks, indices, lengths, frames, values and non-temporal key
+dims bit-exact; turned key dims within 1 bf16 ulp or 2 fp32 ulp).
+
+The draws cover what the fixed cases leave at one value: bf16 and fp32 rows of 16 to 544 bytes (16-byte vectors when a
+row is not a multiple of 32 bytes), 0 to D/2 temporal pairs, ragged chunks (3 to 64 tokens per frame, 1 to 3 frames),
+score rows of 3 to 64 values (scalar and vector scoring paths), 0 to 2 sink chunks, 1 to 3 window chunks, both maps
+g, R and S from the identity to strong compression, the three keep rules, head-specialised steps, paged caches of
+both layouts with several block sizes, and read-time re-indexing (with the final read checked against the oracle's).
+"""
+import numpy as np
+import pytest
+import torch
+
+import autoregressive_video_diffusion_gb300 as dcp
+import oracle
+from oracle import replay
+from synth.workloads import TINY, scaled
+from tests import devcache
+from tests.test_gpu_paged import paged_vs_oracle_step
+from tests.test_gpu_parity import assert_key_parity, gpu_vs_oracle_step
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 32
+
+
+def _clear_of_tie_band(w) -> bool:
+    for c, _, _ in w.evictions():
+        ell = oracle.score(*w.score_inputs(c))
+        if np.min(np.abs(ell.astype(np.float64) - np.float32(w.gamma))) < 1e-6:
+            return False
+    return True
+
+
+def draw(case: int):
+    """A seeded workload and the options of one sweep case: (workload, config overrides, static-head mask or None,
+    (block size, layout) or None)."""
+    r = np.random.default_rng(0x5EE9 + case)
+    dtype = int(r.integers(0, 2))
+    D = int(r.choice([8, 16, 24, 40, 64, 72, 128, 136] if dtype == 0 else [4, 8, 12, 20, 36, 64]))
+    F, T = int(r.integers(1, 4)), int(r.choice([3, 5, 8, 16, 33, 64]))
+    sink, win = int(r.integers(0, 3)), int(r.integers(1, 4))
+    g_mode = int(r.integers(0, 2))
+    R = win * F + int(r.integers(0, 3))
+    S = R + int(r.integers(0, 9)) if g_mode == 0 else int(r.integers(0, 10))
+    n_ev = int(r.integers(1, 6))
+    C = T * F
+    last = sink + n_ev - 1
+    w = scaled(TINY, name=f"sweep_{case}", index=100 + case, L=int(r.integers(1, 4)), H=int(r.integers(1, 6)), D=D,
+               dtype=dtype, n_temporal_pairs=int(r.integers(0, D // 2 + 1)),
+               rope_base=float(r.choice([1e4, 500.0])), tokens_per_frame=T, frames_per_chunk=F,
+               d=int(r.choice([3, 8, 16, 64])), sink_chunks=sink, window_chunks=win, R=float(R), S=float(S),
+               g_mode=g_mode, hist_cap=n_ev * C, max_frames=(last + win + 2) * F, evict_chunk=last,
+               history_chunks=tuple(range(sink, last)), seed=5000 + case)
+    if w.H > 1 and r.random() < 0.3:
+        w = scaled(w, n_static_per_layer=int(r.integers(1, w.H)))
+    over = {"keep_rule": int(r.choice([0, 0, 1, 2])), "random_seed": int(r.integers(0, 1 << 32)),
+            "reindex_mode": int(r.random() < 0.25)}
+    paged = None
+    if r.random() < 0.35:
+        bs = int(r.choice([b for b in (1, 2, 4, 8, 16, 32) if C % b == 0]))
+        paged = (bs, int(r.integers(0, 2)))
+    while not _clear_of_tie_band(w):  # keep every score clear of gamma so both sides take the same decisions
+        w = scaled(w, seed=w.seed + 100)
+    return w, over, w.head_is_static(), paged
+
+
+@pytest.mark.parametrize("case", range(N_CASES))
+def test_sweep_case(gpu, case):
+    w, over, hsm, paged = draw(case)
+    ocfg = replay.cfg_of(w)
+    for key, val in over.items():
+        setattr(ocfg, key, val)
+    hc = replay.new_host_cache(w)
+    placed = set()
+    for ev in w.evictions():
+        for cc in w.resident_window(ev[0]):
+            if cc not in placed:
+                replay.place_chunk(hc, w, cc)
+                placed.add(cc)
+        if paged is None:
+            gpu_vs_oracle_step(w, hc, ev, head_is_static=hsm, **over)
+        else:
+            paged_vs_oracle_step(w, hc, ev, paged[0], paged[1], head_is_static=hsm, seed=case, **over)
+        replay.replay(w, hc, [ev], hsm, placed=placed, cfg=ocfg)  # the host state moves on by the oracle's step
+    if over["reindex_mode"] == 1 and paged is None:
+        q0 = w.evictions()[-1][2]
+        want = oracle.read_history_keys(hc, ocfg, q0)
+        dev = devcache.to_device(hc, w)
+        gcfg = devcache.dcp_config(w, **over)
+        ws = dcp.new_workspace(dcp.dcp_workspace_size(dev, gcfg))
+        out = torch.zeros((w.n_planes, w.hist_cap, w.D), dtype=torch.bfloat16 if w.dtype == 0 else torch.float32,
+                          device="cuda")
+        dcp.dcp_read_history_keys(dev, gcfg, q0, 0, w.n_planes, out, ws)
+        assert dcp.dcp_get_status(dev.status) == dcp.DCP_OK
+        g = out.view(torch.int16).cpu().numpy().view(np.uint16) if w.dtype == 0 else out.cpu().numpy()
+        for pl in range(w.n_planes):
+            n = int(hc.hist_len[pl])
+            assert_key_parity(g[pl, :n], want[pl, :n], w.n_temporal_pairs)

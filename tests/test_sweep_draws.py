@@ -1,0 +1,32 @@
+"""The seeded geometries of the GPU sweep (tests/test_gpu_sweep.py) are valid method inputs: each one's eviction
+schedule replays in the oracle with every step accepted, and the draws reach the variety the sweep claims."""
+import numpy as np
+
+from oracle import replay
+from tests.test_gpu_sweep import N_CASES, draw
+
+
+def test_sweep_draws_replay_in_the_oracle():
+    seen = {"bf16": 0, "fp32": 0, "vec16": 0, "paged": 0, "hs": 0, "lazy": 0, "random": 0, "reverse": 0,
+            "mode1": 0, "no_sink": 0, "scalar_score": 0, "turning": 0}
+    for case in range(N_CASES):
+        w, over, hsm, paged = draw(case)
+        cfg = replay.cfg_of(w)
+        for key, val in over.items():
+            setattr(cfg, key, val)
+        hc = replay.new_host_cache(w)
+        replay.replay(w, hc, w.evictions(), hsm, cfg=cfg)  # asserts every step returns OK
+        assert int(hc.hist_len.max()) <= w.hist_cap
+        seen["bf16" if w.dtype == 0 else "fp32"] += 1
+        seen["vec16"] += (w.D * w.esize) % 32 != 0
+        seen["paged"] += paged is not None
+        seen["hs"] += hsm is not None
+        seen["lazy"] += over["reindex_mode"] == 1
+        seen["random"] += over["keep_rule"] == 2
+        seen["reverse"] += over["keep_rule"] == 1
+        seen["mode1"] += w.g_mode == 1
+        seen["no_sink"] += w.sink_chunks == 0
+        seen["scalar_score"] += w.d % 4 != 0
+        q0_last = w.evictions()[-1][2]
+        seen["turning"] += w.n_temporal_pairs > 0 and (q0_last - w.sink_chunks * w.F) > (w.S if w.g_mode == 0 else w.R + w.S)
+    assert all(v > 0 for v in seen.values()), seen
