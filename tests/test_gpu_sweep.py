@@ -7,6 +7,8 @@ row is not a multiple of 32 bytes), 0 to D/2 temporal pairs, ragged chunks (3 to
 score rows of 3 to 64 values (scalar and vector scoring paths), 0 to 2 sink chunks, 1 to 3 window chunks, both maps
 g, R and S from the identity to strong compression, the three keep rules, head-specialised steps, paged caches of
 both layouts with several block sizes, and read-time re-indexing (with the final read checked against the oracle's).
+Wide draws (1024 to 1600 planes, rows of at most 288 bytes, short chunks) run steps that turn no kept key on the
+shared-memory staged gather, across row sizes and dtypes, and steps that turn on the register-staged gather.
 """
 import numpy as np
 import pytest
@@ -22,7 +24,7 @@ from tests.test_gpu_parity import assert_key_parity, gpu_vs_oracle_step
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 32
+N_CASES = 48
 
 
 def _clear_of_tie_band(w) -> bool:
@@ -66,9 +68,40 @@ def draw(case: int):
     return w, over, w.head_is_static(), paged
 
 
-@pytest.mark.parametrize("case", range(N_CASES))
+def draw_wide(case: int):
+    """A seeded workload of 1024 to 1600 planes with short chunks and rows of at most 288 bytes: the caches on which
+    steps whose kept keys do not turn take the shared-memory staged gather."""
+    r = np.random.default_rng(0x91DE + case)
+    dtype = int(r.integers(0, 2))
+    D = int(r.choice([8, 16, 64, 72, 128, 136] if dtype == 0 else [4, 20, 36, 64, 72]))
+    F, T = int(r.integers(1, 3)), int(r.choice([3, 8, 16]))
+    sink, win = int(r.integers(0, 3)), int(r.integers(1, 4))
+    R = win * F + int(r.integers(0, F))  # below (w + 1) F: the leaving chunk's oldest frames lie past R
+    S = R + int(r.choice([0, 2, 30]))
+    n_ev = int(r.integers(1, 4))
+    last = sink + n_ev - 1
+    w = scaled(TINY, name=f"sweep_wide_{case}", index=200 + case, L=int(r.choice([32, 40])),
+               H=int(r.choice([32, 40])), D=D, dtype=dtype, n_temporal_pairs=int(r.integers(0, D // 2 + 1)),
+               tokens_per_frame=T, frames_per_chunk=F, d=int(r.choice([3, 16])), sink_chunks=sink,
+               window_chunks=win, R=float(R), S=float(S), g_mode=0, hist_cap=n_ev * T * F,
+               max_frames=(last + win + 2) * F, evict_chunk=last, history_chunks=tuple(range(sink, last)),
+               seed=7000 + case)
+    if r.random() < 0.4:
+        w = scaled(w, n_static_per_layer=int(r.integers(1, w.H)))
+    over = {"keep_rule": int(r.choice([0, 1, 2])), "random_seed": int(r.integers(0, 1 << 32)), "reindex_mode": 0}
+    while not _clear_of_tie_band(w):
+        w = scaled(w, seed=w.seed + 100)
+    return w, over, w.head_is_static(), None
+
+
+N_WIDE = 8
+
+
+@pytest.mark.parametrize("case", [("narrow", i) for i in range(N_CASES)] + [("wide", i) for i in range(N_WIDE)],
+                         ids=[f"case{i}" for i in range(N_CASES)] + [f"wide{i}" for i in range(N_WIDE)])
 def test_sweep_case(gpu, case):
-    w, over, hsm, paged = draw(case)
+    kind, case = case
+    w, over, hsm, paged = draw(case) if kind == "narrow" else draw_wide(case)
     ocfg = replay.cfg_of(w)
     for key, val in over.items():
         setattr(ocfg, key, val)

@@ -3,7 +3,7 @@ schedule replays in the oracle with every step accepted, and the draws reach the
 import numpy as np
 
 from oracle import replay
-from tests.test_gpu_sweep import N_CASES, draw
+from tests.test_gpu_sweep import N_CASES, N_WIDE, draw, draw_wide
 
 
 def test_sweep_draws_replay_in_the_oracle():
@@ -30,3 +30,23 @@ def test_sweep_draws_replay_in_the_oracle():
         q0_last = w.evictions()[-1][2]
         seen["turning"] += w.n_temporal_pairs > 0 and (q0_last - w.sink_chunks * w.F) > (w.S if w.g_mode == 0 else w.R + w.S)
     assert all(v > 0 for v in seen.values()), seen
+
+
+def test_wide_draws_replay_in_the_oracle():
+    """The wide draws (1024+ planes, rows of at most 288 bytes) replay in the oracle, and some of their steps turn no
+    kept key (the staged gather) while others turn (the register-staged one)."""
+    still = turning = 0
+    for case in range(N_WIDE):
+        w, over, hsm, _ = draw_wide(case)
+        assert w.n_planes >= 1024 and w.D * w.esize <= 288 and (w.D * w.esize) % 16 == 0
+        cfg = replay.cfg_of(w)
+        for key, val in over.items():
+            setattr(cfg, key, val)
+        hc = replay.new_host_cache(w)
+        replay.replay(w, hc, w.evictions(), hsm, cfg=cfg)
+        for c, _, q0 in w.evictions():
+            # the leaving chunk's keys turn iff its offsets reach past R while g compresses (mode 0: q0 - T_s > S)
+            turns = w.n_temporal_pairs > 0 and q0 - w.sink_chunks * w.F > w.S and q0 - c * w.F > w.R
+            turning += turns
+            still += not turns
+    assert still > 0 and turning > 0, (still, turning)
