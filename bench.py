@@ -72,34 +72,104 @@ def _peaks():
 
 
 # ------------------------------------------------------------------------------------------ clocks
+class _Nvml:
+    """Reads (never sets) one GPU's SM clock, its maximum and the active clock-event reasons through NVML."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, local: int):
+        import ctypes
+        import torch
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(local)
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:  # the physical GPU behind this process's device (CUDA_VISIBLE_DEVICES may renumber)
+            rc = lib.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(), ctypes.byref(self.h))
+        else:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(local, ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle")
+        self.lib = lib
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_mhz = self._clock(lib.nvmlDeviceGetMaxClockInfo)
+
+    def _clock(self, fn):
+        v = self.ct.c_uint()
+        if fn(self.h, 1, self.ct.byref(v)) != 0:  # NVML_CLOCK_SM
+            raise OSError("clock query failed")
+        return float(v.value)
+
+    def read(self):
+        r = self.ct.c_ulonglong()
+        if self.reasons_fn(self.h, self.ct.byref(r)) != 0:
+            raise OSError("reason query failed")
+        return self._clock(self.lib.nvmlDeviceGetClockInfo), self.max_mhz, \
+            {n for b, n in self.REASONS.items() if r.value & b}
+
+
 class ClockSampler:
+    """SM clock and throttle reasons while the bench runs: NVML polled every 2 ms (reads only), so that the short
+    timed region gets samples of its own; nvidia-smi's 50 ms loop where NVML cannot be loaded."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    SMI_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu_index = gpu_index
         self.proc = None
-        self.lines = []
+        self.rows = []  # (time, sm MHz, max MHz, set of active reasons)
         self.marks = []
+        self.source = None
+        self._stop = threading.Event()
 
     def start(self):
+        try:
+            nv = _Nvml(self.gpu_index)
+            self.source = "nvml, 2 ms"
+            threading.Thread(target=self._poll, args=(nv,), daemon=True).start()
+            return
+        except (OSError, AttributeError):
+            pass
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-i", str(self.gpu_index), "-lms", "50"], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, 50 ms"
             threading.Thread(target=self._read, daemon=True).start()
         except OSError:
             self.proc = None
 
+    def _poll(self, nv):
+        while not self._stop.is_set():
+            try:
+                sm, mx, reasons = nv.read()
+            except OSError:
+                return
+            self.rows.append((time.time(), sm, mx, reasons))
+            time.sleep(0.002)
+
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append((time.time(), ln.strip()))
+            parts = [x.strip() for x in ln.strip().split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                row = (time.time(), float(parts[1]), float(parts[2]),
+                       {n for n, v in zip(self.SMI_REASONS, parts[5:9]) if v.lower() == "active"})
+            except ValueError:
+                continue
+            self.rows.append(row)
 
     def mark(self, name):
         self.marks.append((name, time.time()))
 
     def stop(self):
+        self._stop.set()
         if self.proc:
             self.proc.terminate()
             try:
@@ -108,27 +178,17 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0, t1):
-        rows = []
-        for ts, ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
-            except ValueError:
-                continue
+        rows = list(self.rows)
         inside = [r for r in rows if t0 <= r[0] <= t1]
         use = inside if len(inside) >= 3 else [r for r in rows if r[0] <= t1]
         if not use:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"], "samples": 0}
         reasons = set()
         for r in use:
-            for n, v in zip(names[1:], r[3][1:]):
-                if v.lower() == "active":
-                    reasons.add(n)
+            reasons |= r[3]
         return {"sm_mhz": float(np.median([r[1] for r in use])), "sm_max_mhz": max(r[2] for r in use),
-                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside),
+                "source": self.source}
 
 
 # ------------------------------------------------------------------------------------------ distributed
