@@ -130,7 +130,10 @@ ScanParams cache_scan_params(const dcp_cache* c, const dcp_config* g, const Deri
 
 void finish_tables(ScanParams& sp) {
   const int entries = (sp.g_frames + (sp.h_hi - sp.h_lo)) * sp.n_t;
-  sp.n_trig_blocks = (entries + kTableEntries - 1) / kTableEntries;
+  int per = (entries + kTableTargetCTAs - 1) / kTableTargetCTAs;
+  per = per < kTableMinEntries ? kTableMinEntries : (per > kTableEntries ? kTableEntries : per);
+  sp.tbl_per = per;
+  sp.n_trig_blocks = (entries + per - 1) / per;
 }
 
 // 32-byte vector accesses need 32-byte aligned rows and bases; otherwise the kernels use 16-byte vectors.

@@ -98,8 +98,8 @@ struct ScanParams {
   const int32_t* tbl_b;
   int32_t n_tbl_a, n_tbl_b, n_tbl_slices;
   int64_t n_blocks;
-  // phase tables, built by the CTAs numbered past the tiles (kTableEntries entries each)
-  int32_t n_trig_blocks;
+  // phase tables, built by the CTAs numbered past the tiles (tbl_per entries each, at most kTableEntries)
+  int32_t n_trig_blocks, tbl_per;
   float4* trig_g;          // [F][n_t]: turn from t to t~(t; q0) for the leaving chunk's frames
   uint8_t* rot_g;          // [F]: nonzero if that frame turns at all
   int32_t g_frames;        // F, or 0 when no gather follows (read-time re-index: frames [T_s, q0))
@@ -115,7 +115,12 @@ struct ScanParams {
   int32_t q0, q0_prev;
 };
 
-constexpr int kTableEntries = 64;  // table entries per table CTA (fp64 work spread over many SMs)
+// Table entries per table CTA: at most kTableEntries, at least kTableMinEntries, spread over about
+// kTableTargetCTAs CTAs.  GB300 runs fp64 at a small fraction of its fp32 rate, so one entry (an exp2, the phase map's
+// divisions, a sincos) takes microseconds of one SM's fp64 pipe; short tables spread thinly finish sooner.
+constexpr int kTableEntries = 64;
+constexpr int kTableMinEntries = 8;
+constexpr int kTableTargetCTAs = 128;
 // The streaming kernels move 64 bytes per thread, tensor and plane: four 16-byte vectors, or two 32-byte vectors
 // when rows and base addresses are 32-byte aligned.
 constexpr int kBytesPerThread = 64;

@@ -182,9 +182,9 @@ __device__ void table_checks(const ScanParams& p, int slice) {
 // theta_p = base^(-p / n_t) is evaluated as exp2(log2(base) * (-p / n_t)): the same value to a few ulps of fp64,
 // far below the 2^-48 carried by the table, and much cheaper than pow on a part with a low fp64 rate.
 __device__ void table_work(const ScanParams& p, int block) {
-  if (threadIdx.x >= kTableEntries) return;
+  if (threadIdx.x >= p.tbl_per) return;
   const double log2_base = log2(p.base);
-  const int e = block * kTableEntries + threadIdx.x;
+  const int e = block * p.tbl_per + threadIdx.x;
   const int n_g = p.g_frames * p.n_t;
   const int n_h = (p.h_hi - p.h_lo) * p.n_t;
   if (e < n_g) {
