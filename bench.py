@@ -924,12 +924,14 @@ def main():
     ap.add_argument("--tokens-per-frame", type=int, default=0,
                     help="profiling captures only: the same workload with shorter chunks (every plane kept, a few GB)")
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before the timed region")
-    ap.add_argument("--case", default="step", choices=["step", "reindex", "score", "random", "read", "snapshot"],
+    ap.add_argument("--case", default="step",
+                    choices=["step", "reindex", "score", "random", "read", "snapshot", "paged-hnd", "paged-nhd"],
                     help="step: the prune step (default); reindex: dcp_rope_reindex of a 64-plane cache with 90,000 "
                          "history rows per plane; score: dcp_score_mask of one full-depth chunk (random: under "
                          "keep rule 2); read: dcp_read_history_keys of the re-index case's history; snapshot: "
                          "dcp_snapshot / dcp_restore of the state after the full-depth eviction cut to --layers "
-                         "(default 8) layers")
+                         "(default 8) layers; paged-hnd / paged-nhd: the full-depth step on a paged copy of the "
+                         "cache (16-position blocks)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -938,6 +940,20 @@ def main():
         __graft_entry__.build()
         from synth.workloads import FULL, scaled
         print(json.dumps({"case": "snapshot", **run_snapshot(scaled(FULL, L=args.layers or 8), reps=args.steps)}))
+        return
+    if args.case.startswith("paged-"):
+        import __graft_entry__
+        __graft_entry__.build()
+        import autoregressive_video_diffusion_gb300 as dcp
+        from synth.workloads import FULL, scaled
+        wp = FULL if args.layers <= 0 else scaled(FULL, L=args.layers, name=f"{FULL.name}_L{args.layers}")
+        layout = dcp.DCP_PAGED_HND if args.case == "paged-hnd" else dcp.DCP_PAGED_NHD
+        r = run_gpu(wp, args.steps, args.warmup, 1, 0, 0, None, e2e_steps=0, preroll_s=args.preroll,
+                    paged=(16, layout))
+        print(json.dumps({"case": args.case, "workload": wp.name, "block_size": 16, "kept": r["k"],
+                          "us_per_step": r["ms"] * 1e3, "GB_per_s": r["alg_bytes"] / (r["ms"] * 1e-3) / 1e9,
+                          "gather_us": r["gather_ms"] * 1e3,
+                          "gather_GB_per_s": r["gather_bytes"] / (r["gather_ms"] * 1e-3) / 1e9}))
         return
     if args.case != "step":
         run_entry_case(args.case, args.steps, args.warmup)
