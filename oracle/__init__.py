@@ -97,7 +97,7 @@ def _p(a):
 
 @dataclass
 class Cfg:
-    """Method parameters (page readings are documented in the design doc)."""
+    """Method parameters; the readings of the points the page leaves open are listed at the top of dcp_oracle.cpp."""
     gamma: float = 0.10
     keep_rule: int = 0
     sink_chunks: int = 1

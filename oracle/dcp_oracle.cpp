@@ -11,7 +11,7 @@
 //   [limits] 전제와 한계 "premises and limits" - the 4-step schedule (999, 957, 899, 702), probe index 2, gamma 0.10.
 //
 // Style: one thread, plain loops, fp64 arithmetic, one rounding to the storage type at the end of each value.
-// Readings of points the page leaves open (each listed in the design doc):
+// Readings of points the page leaves open (the CUDA path takes the same ones):
 //   * keep rule: keep when l > gamma (strict), drop otherwise; the reverse criterion is the complement; the Random
 //     ablation keeps the same number of tokens, drawn uniformly without replacement from a SplitMix64 stream.
 //   * pair p of the temporal RoPE sub-vector occupies dims (2p, 2p+1); theta_p = base^(-p / n_t).

@@ -1,6 +1,6 @@
 """GPU parity: the CUDA prune step (through the C ABI) against the CPU oracle on the same seeded inputs.
 
-Bars (written here, derived in the design doc): masks, index lists, kept counts, hist_len, hist_t, every value row and every
+Bars: masks, index lists, kept counts, hist_len, hist_t, every value row and every
 non-temporal key dim are bit-exact; l is within 1e-5 relative; re-phased keys are within 1 bf16 ulp (2 fp32 ulp) of
 the oracle's fp64 rotation rounded once.  The masks are compared exactly because every seeded input keeps
 |l - gamma| >= 1e-6 (checked on the CPU in test_abi.py).
