@@ -8,7 +8,8 @@ score rows of 3 to 64 values (scalar and vector scoring paths), 0 to 2 sink chun
 g, R and S from the identity to strong compression, the three keep rules, head-specialised steps, paged caches of
 both layouts with several block sizes, and read-time re-indexing (with the final read checked against the oracle's).
 Wide draws (1024 to 1600 planes, rows of at most 288 bytes, short chunks) run steps that turn no kept key on the
-shared-memory staged gather, across row sizes and dtypes, and steps that turn on the register-staged gather.
+shared-memory staged gather, across row sizes and dtypes, and steps that turn on the register-staged gather; some of
+them run on paged pools (HND or NHD, 8 to 32 positions per block), which take the register-staged gather.
 """
 import numpy as np
 import pytest
@@ -89,9 +90,13 @@ def draw_wide(case: int):
     if r.random() < 0.4:
         w = scaled(w, n_static_per_layer=int(r.integers(1, w.H)))
     over = {"keep_rule": int(r.choice([0, 1, 2])), "random_seed": int(r.integers(0, 1 << 32)), "reindex_mode": 0}
+    paged = None
+    sizes = [b for b in (8, 16, 32) if (T * F) % b == 0]
+    if sizes and r.random() < 0.5:  # paged pools of many planes
+        paged = (int(r.choice(sizes)), int(r.choice([0, 0, 1])))
     while not _clear_of_tie_band(w):
         w = scaled(w, seed=w.seed + 100)
-    return w, over, w.head_is_static(), None
+    return w, over, w.head_is_static(), paged
 
 
 N_WIDE = 8

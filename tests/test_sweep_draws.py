@@ -35,9 +35,10 @@ def test_sweep_draws_replay_in_the_oracle():
 def test_wide_draws_replay_in_the_oracle():
     """The wide draws (1024+ planes, rows of at most 288 bytes) replay in the oracle, and some of their steps turn no
     kept key (the staged gather) while others turn (the register-staged one)."""
-    still = turning = 0
+    still = turning = n_paged = 0
     for case in range(N_WIDE):
-        w, over, hsm, _ = draw_wide(case)
+        w, over, hsm, paged = draw_wide(case)
+        n_paged += paged is not None
         assert w.n_planes >= 1024 and w.D * w.esize <= 288 and (w.D * w.esize) % 16 == 0
         cfg = replay.cfg_of(w)
         for key, val in over.items():
@@ -49,4 +50,4 @@ def test_wide_draws_replay_in_the_oracle():
             turns = w.n_temporal_pairs > 0 and q0 - w.sink_chunks * w.F > w.S and q0 - c * w.F > w.R
             turning += turns
             still += not turns
-    assert still > 0 and turning > 0, (still, turning)
+    assert still > 0 and turning > 0 and n_paged > 0, (still, turning, n_paged)
