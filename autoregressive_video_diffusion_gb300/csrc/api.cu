@@ -1,5 +1,6 @@
 // Host side of libdcp: argument validation, workspace layout and the launch sequence of each entry point.
 // The entry points and their contracts are documented in include/dcp.h.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -399,13 +400,17 @@ SnapParams snap_params(const dcp_cache* c, const dcp_config* g, const Derived& d
 
 namespace dcp {
 int sm_count() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[kMaxDevices];  // zero until first read on that device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached) {
+    const int n = cache[dev].load(std::memory_order_relaxed);
+    if (n) return n;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (cached) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 }  // namespace dcp

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/dcp.h"
 
 namespace dcp {
@@ -236,9 +238,11 @@ cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_
 int sm_count();
 
 // Per-device launch set-up of one kernel, made on first use on each device: the dynamic shared-memory opt-in (a
-// per-device function attribute) and the number of CTAs that fit on an SM with that much shared memory.
+// per-device function attribute) and the number of CTAs that fit on an SM with that much shared memory.  Host
+// threads that launch on different caches share it, so it is updated under a mutex (the opt-in must only grow).
 constexpr int kMaxDevices = 64;
 struct LaunchCache {
+  std::mutex m;
   size_t opted[kMaxDevices];    // dynamic shared memory opted in so far (bytes)
   size_t counted[kMaxDevices];  // shared-memory size + 1 that blocks[] was computed for (0: not yet)
   int blocks[kMaxDevices];
@@ -248,6 +252,7 @@ template <typename Kernel>
 cudaError_t launch_setup(LaunchCache& lc, Kernel kernel, int threads, size_t smem, int* blocks_per_sm) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> guard(lc.m);
   if (smem > 48 * 1024 && smem > lc.opted[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -25,7 +25,8 @@
  *     only that row is left unturned.
  *   - The workspace is caller-owned device scratch of dcp_workspace_size() bytes, 256-byte aligned.  Zero it once
  *     with dcp_workspace_init() before its first use; every call leaves it ready for the next.  Calls that share a
- *     workspace or a cache must be ordered on one stream (not thread-safe per workspace or cache).
+ *     workspace or a cache must be ordered on one stream (not thread-safe per workspace or cache).  Host threads
+ *     may call the library at the same time on different caches and workspaces (on one or several devices).
  *
  * KV cache layout (dcp_cache): K and V are [L][H][cap][D] arrays (bf16 or fp32), row-major, one plane of cap rows
  * per (layer, head).  Rows of a plane are laid out as
