@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one full-depth gather launch (gather_staged_kernel) from the ncu capture summarised in
 # profiles/gather_kernel_full_depth_dram.md.  They describe the kernel sources they were taken on: when the hash of
 # those sources differs, the bench reports no traffic figure.
-GATHER_TRAFFIC_BYTES = 1_504_016_384
-GATHER_TRAFFIC_SOURCES_SHA256 = "bddf5484d99d4797797f9c17f5cb3a324ebade70b19cd98ccb290aff39ba3a73"
+GATHER_TRAFFIC_BYTES = 1_503_282_432
+GATHER_TRAFFIC_SOURCES_SHA256 = "7a70e3aec16efe017e28ea5a7379fa510deefd84d5e8a0ad0270183ab437f884"
 
 
 def _gather_traffic():
