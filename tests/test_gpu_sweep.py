@@ -9,7 +9,8 @@ g, R and S from the identity to strong compression, the three keep rules, head-s
 both layouts with several block sizes, and read-time re-indexing (with the final read checked against the oracle's).
 Wide draws (1024 to 1600 planes, rows of at most 288 bytes, short chunks) run steps that turn no kept key on the
 shared-memory staged gather, across row sizes and dtypes, and steps that turn on the register-staged gather; some of
-them run on paged pools (HND or NHD, 8 to 32 positions per block), which take the register-staged gather.
+them run on paged pools (HND or NHD, 8 to 32 positions per block), which take the register-staged gather.  Big
+draws use rows of 1 to 4 KiB (the largest the library takes) with up to 1024 temporal pairs.
 """
 import numpy as np
 import pytest
@@ -102,11 +103,40 @@ def draw_wide(case: int):
 N_WIDE = 8
 
 
-@pytest.mark.parametrize("case", [("narrow", i) for i in range(N_CASES)] + [("wide", i) for i in range(N_WIDE)],
-                         ids=[f"case{i}" for i in range(N_CASES)] + [f"wide{i}" for i in range(N_WIDE)])
+def draw_big(case: int):
+    """A seeded workload with long rows (1 to 4 KiB, the largest the library takes) and long temporal parts: few
+    rows per CTA in every kernel, many vectors per row."""
+    r = np.random.default_rng(0xB16 + case)
+    dtype = int(r.integers(0, 2))
+    D = int(r.choice([512, 1024, 2048] if dtype == 0 else [256, 512, 1024]))
+    F, T = int(r.integers(1, 3)), int(r.choice([4, 9, 16]))
+    win = int(r.integers(1, 3))
+    R = win * F + int(r.integers(0, F))
+    S = R + int(r.choice([0, 3]))
+    n_ev = int(r.integers(2, 5))
+    last = 1 + n_ev - 1
+    n_t = int(r.integers(1, min(D // 2, 1024 // F) + 1))  # the gather keeps F x n_t table entries in shared memory
+    w = scaled(TINY, name=f"sweep_big_{case}", index=300 + case, L=int(r.integers(1, 3)), H=int(r.integers(1, 4)),
+               D=D, dtype=dtype, n_temporal_pairs=n_t, tokens_per_frame=T, frames_per_chunk=F, d=16, sink_chunks=1,
+               window_chunks=win, R=float(R), S=float(S), g_mode=0, hist_cap=n_ev * T * F,
+               max_frames=(last + win + 2) * F, evict_chunk=last, history_chunks=tuple(range(1, last)),
+               seed=9000 + case)
+    over = {"keep_rule": 0, "random_seed": 0, "reindex_mode": int(r.random() < 0.3)}
+    while not _clear_of_tie_band(w):
+        w = scaled(w, seed=w.seed + 100)
+    return w, over, None, None
+
+
+N_BIG = 6
+
+
+@pytest.mark.parametrize("case", [("narrow", i) for i in range(N_CASES)] + [("wide", i) for i in range(N_WIDE)] +
+                         [("big", i) for i in range(N_BIG)],
+                         ids=[f"case{i}" for i in range(N_CASES)] + [f"wide{i}" for i in range(N_WIDE)] +
+                         [f"big{i}" for i in range(N_BIG)])
 def test_sweep_case(gpu, case):
     kind, case = case
-    w, over, hsm, paged = draw(case) if kind == "narrow" else draw_wide(case)
+    w, over, hsm, paged = {"narrow": draw, "wide": draw_wide, "big": draw_big}[kind](case)
     ocfg = replay.cfg_of(w)
     for key, val in over.items():
         setattr(ocfg, key, val)

@@ -3,7 +3,7 @@ schedule replays in the oracle with every step accepted, and the draws reach the
 import numpy as np
 
 from oracle import replay
-from tests.test_gpu_sweep import N_CASES, N_WIDE, draw, draw_wide
+from tests.test_gpu_sweep import N_BIG, N_CASES, N_WIDE, draw, draw_big, draw_wide
 
 
 def test_sweep_draws_replay_in_the_oracle():
@@ -51,3 +51,19 @@ def test_wide_draws_replay_in_the_oracle():
             turning += turns
             still += not turns
     assert still > 0 and turning > 0 and n_paged > 0, (still, turning, n_paged)
+
+
+def test_big_draws_replay_in_the_oracle():
+    """The big-row draws are valid (rows of at most 4 KiB, the gather's table fits) and replay in the oracle."""
+    sizes = set()
+    for case in range(N_BIG):
+        w, over, hsm, _ = draw_big(case)
+        rb = w.D * w.esize
+        assert 1024 <= rb <= 4096 and rb % 16 == 0 and w.F * w.n_temporal_pairs * 16 <= 100 * 1024
+        sizes.add(rb)
+        cfg = replay.cfg_of(w)
+        for key, val in over.items():
+            setattr(cfg, key, val)
+        hc = replay.new_host_cache(w)
+        replay.replay(w, hc, w.evictions(), hsm, cfg=cfg)
+    assert len(sizes) >= 2, sizes
