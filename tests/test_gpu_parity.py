@@ -279,6 +279,16 @@ def test_capacity_error_leaves_cache(gpu):
     assert np.array_equal(before.k, after.k) and np.array_equal(before.hist_len, after.hist_len)
 
 
+def test_history_filled_exactly(gpu):
+    """Every token kept at every eviction with a history region of exactly the rows they need: the last step fills it
+    to hist_cap and is accepted (the capacity bound is inclusive)."""
+    w = scaled(TINY_ROT, gamma=-1.0, hist_cap=5 * 64)
+    hc, ev = replay.state_before_last(w)
+    assert int(hc.hist_len[0]) + w.C == w.hist_cap
+    o, g, idx, _ = gpu_vs_oracle_step(w, hc, ev)
+    assert len(idx) == w.C and int(g.hist_len[0]) == w.hist_cap
+
+
 def test_inconsistent_lengths_detected(gpu):
     w = TINY_ROT
     hc, (c, q0_prev, q0) = replay.state_before_last(w)
