@@ -84,7 +84,7 @@ def test_workspace_size():
 
 @pytest.mark.parametrize("bad", [
     dict(k=0), dict(v=0), dict(hist_len=0), dict(hist_t=0), dict(status=0), dict(k=FAKE + 8), dict(L=0), dict(H=0),
-    dict(D=0), dict(D=127), dict(D=4), dict(dtype=7), dict(cap=6240 * 5), dict(hist_cap=-1)])
+    dict(D=0), dict(D=127), dict(D=4), dict(D=2056), dict(dtype=7), dict(cap=6240 * 5), dict(hist_cap=-1)])
 def test_invalid_cache_rejected(bad):
     assert _ws_size(_cache(**bad), _cfg()) == 0
 

@@ -10,7 +10,8 @@ both layouts with several block sizes, and read-time re-indexing (with the final
 Wide draws (1024 to 1600 planes, rows of at most 288 bytes, short chunks) run steps that turn no kept key on the
 shared-memory staged gather, across row sizes and dtypes, and steps that turn on the register-staged gather; some of
 them run on paged pools (HND or NHD, 8 to 32 positions per block), which take the register-staged gather.  Big
-draws use rows of 1 to 4 KiB (the largest the library takes) with up to 1024 temporal pairs.
+draws use rows of 1 to 4 KiB (the largest the library takes) with up to 1024 temporal pairs; edge draws use chunks of
+1 to 33 tokens and score rows of 1 to 64 values.
 """
 import numpy as np
 import pytest
@@ -129,14 +130,41 @@ def draw_big(case: int):
 
 N_BIG = 6
 
+# degenerate chunks: (tokens per frame, frames per chunk, score width)
+EDGE = [(1, 1, 1), (1, 3, 2), (2, 1, 3), (31, 1, 4), (33, 1, 5), (1, 2, 64)]
+
+
+def draw_edge(case: int):
+    """Chunks of 1 to 33 tokens and score rows of 1 to 64 values: a tile holds part of one warp, the ballot words a
+    few bits."""
+    r = np.random.default_rng(0xED6E + case)
+    T, F, d = EDGE[case]
+    win = int(r.integers(1, 3))
+    R = win * F + int(r.integers(0, 2))
+    n_ev = int(r.integers(2, 6))
+    last = 1 + n_ev - 1
+    w = scaled(TINY, name=f"sweep_edge_{case}", index=400 + case, L=2, H=2, D=16, dtype=int(r.integers(0, 2)),
+               n_temporal_pairs=int(r.integers(1, 9)), tokens_per_frame=T, frames_per_chunk=F, d=d, sink_chunks=1,
+               window_chunks=win, R=float(R), S=float(R), g_mode=0, hist_cap=n_ev * T * F,
+               max_frames=(last + win + 2) * F, evict_chunk=last, history_chunks=tuple(range(1, last)),
+               seed=9500 + case)
+    over = {"keep_rule": int(r.choice([0, 1, 2])), "random_seed": int(r.integers(0, 1 << 32)),
+            "reindex_mode": int(r.random() < 0.3)}
+    while not _clear_of_tie_band(w):
+        w = scaled(w, seed=w.seed + 100)
+    return w, over, None, None
+
+
+N_EDGE = len(EDGE)
+
 
 @pytest.mark.parametrize("case", [("narrow", i) for i in range(N_CASES)] + [("wide", i) for i in range(N_WIDE)] +
-                         [("big", i) for i in range(N_BIG)],
+                         [("big", i) for i in range(N_BIG)] + [("edge", i) for i in range(N_EDGE)],
                          ids=[f"case{i}" for i in range(N_CASES)] + [f"wide{i}" for i in range(N_WIDE)] +
-                         [f"big{i}" for i in range(N_BIG)])
+                         [f"big{i}" for i in range(N_BIG)] + [f"edge{i}" for i in range(N_EDGE)])
 def test_sweep_case(gpu, case):
     kind, case = case
-    w, over, hsm, paged = {"narrow": draw, "wide": draw_wide, "big": draw_big}[kind](case)
+    w, over, hsm, paged = {"narrow": draw, "wide": draw_wide, "big": draw_big, "edge": draw_edge}[kind](case)
     ocfg = replay.cfg_of(w)
     for key, val in over.items():
         setattr(ocfg, key, val)

@@ -3,7 +3,7 @@ schedule replays in the oracle with every step accepted, and the draws reach the
 import numpy as np
 
 from oracle import replay
-from tests.test_gpu_sweep import N_BIG, N_CASES, N_WIDE, draw, draw_big, draw_wide
+from tests.test_gpu_sweep import N_BIG, N_CASES, N_EDGE, N_WIDE, draw, draw_big, draw_edge, draw_wide
 
 
 def test_sweep_draws_replay_in_the_oracle():
@@ -67,3 +67,15 @@ def test_big_draws_replay_in_the_oracle():
         hc = replay.new_host_cache(w)
         replay.replay(w, hc, w.evictions(), hsm, cfg=cfg)
     assert len(sizes) >= 2, sizes
+
+
+def test_edge_draws_replay_in_the_oracle():
+    """The degenerate-chunk draws (1 to 33 tokens, score rows of 1 to 64 values) replay in the oracle."""
+    for case in range(N_EDGE):
+        w, over, hsm, _ = draw_edge(case)
+        assert 1 <= w.C <= 33
+        cfg = replay.cfg_of(w)
+        for key, val in over.items():
+            setattr(cfg, key, val)
+        hc = replay.new_host_cache(w)
+        replay.replay(w, hc, w.evictions(), hsm, cfg=cfg)
