@@ -6,7 +6,8 @@ The draws cover what the fixed cases leave at one value: bf16 and fp32 rows of 1
 row is not a multiple of 32 bytes), 0 to D/2 temporal pairs, ragged chunks (3 to 64 tokens per frame, 1 to 3 frames),
 score rows of 3 to 64 values (scalar and vector scoring paths), 0 to 2 sink chunks, 1 to 3 window chunks, both maps
 g, R and S from the identity to strong compression, the three keep rules, head-specialised steps, paged caches of
-both layouts with several block sizes, and read-time re-indexing (with the final read checked against the oracle's).
+both layouts with several block sizes, and read-time re-indexing (with the final read, contiguous or paged, checked
+against the oracle's).
 Wide draws (1024 to 1600 planes, rows of at most 288 bytes, short chunks) run steps that turn no kept key on the
 shared-memory staged gather, across row sizes and dtypes, and steps that turn on the register-staged gather; some of
 them run on paged pools (HND or NHD, 8 to 32 positions per block), which take the register-staged gather.  Big
@@ -22,6 +23,7 @@ import oracle
 from oracle import replay
 from synth.workloads import TINY, scaled
 from tests import devcache
+from tests.paged import PagedCopy
 from tests.test_gpu_paged import paged_vs_oracle_step
 from tests.test_gpu_parity import assert_key_parity, gpu_vs_oracle_step
 
@@ -180,16 +182,18 @@ def test_sweep_case(gpu, case):
         else:
             paged_vs_oracle_step(w, hc, ev, paged[0], paged[1], head_is_static=hsm, seed=case, **over)
         replay.replay(w, hc, [ev], hsm, placed=placed, cfg=ocfg)  # the host state moves on by the oracle's step
-    if over["reindex_mode"] == 1 and paged is None:
+    if over["reindex_mode"] == 1:  # the read of the final history at the last q0, contiguous or paged
         q0 = w.evictions()[-1][2]
         want = oracle.read_history_keys(hc, ocfg, q0)
         dev = devcache.to_device(hc, w)
         gcfg = devcache.dcp_config(w, **over)
-        ws = dcp.new_workspace(dcp.dcp_workspace_size(dev, gcfg))
+        src = dev if paged is None else PagedCopy(dev, gcfg, paged[0], paged[1], seed=case + 1).cache
+        size = dcp.dcp_workspace_size(dev, gcfg) if paged is None else dcp.dcp_paged_workspace_size(src, gcfg)
+        ws = dcp.new_workspace(size)
         out = torch.zeros((w.n_planes, w.hist_cap, w.D), dtype=torch.bfloat16 if w.dtype == 0 else torch.float32,
                           device="cuda")
-        dcp.dcp_read_history_keys(dev, gcfg, q0, 0, w.n_planes, out, ws)
-        assert dcp.dcp_get_status(dev.status) == dcp.DCP_OK
+        dcp.dcp_read_history_keys(src, gcfg, q0, 0, w.n_planes, out, ws)
+        assert dcp.dcp_get_status(src.status) == dcp.DCP_OK
         g = out.view(torch.int16).cpu().numpy().view(np.uint16) if w.dtype == 0 else out.cpu().numpy()
         for pl in range(w.n_planes):
             n = int(hc.hist_len[pl])
