@@ -197,8 +197,13 @@ dcp_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? DCP_OK : DCP_ECUDA
 
 // No kept key of the leaving chunk changes phase: g is the identity on every offset q0 - t of the chunk's frames, which
 // holds when the oldest non-sink offset already fits the span (g is then the identity everywhere) or when the chunk's
-// oldest offset is within the recent range R.  Read-time re-index moves keys unturned.  Used only to pick the
-// gather's form (both forms turn whatever the tables say), so it is a speed choice, never a correctness one.
+// oldest offset is within the recent range R.  Read-time re-index moves keys unturned.
+// This decision is load-bearing, not only a choice of speed: when it holds, the scan builds no cos/sin table for the
+// chunk and no gather form turns any key (the staged form cannot turn; the register-staged one skips its turn under
+// no_turn).  It is exact because it restates g's closed form: g(delta) = delta for delta <= R, and everywhere when
+// delta_max = q0 - T_s <= span end, so t~(t) = t for every frame of the chunk (the chunk's oldest offset is
+// q0 - evict_first_frame, its largest).  The GPU sweep draws steps on both sides of each boundary
+// (q0 - evict_first_frame = R, R + 1; q0 - T_s = span end, span end + 1) and compares them with the oracle.
 bool chunk_keeps_phase(const dcp_config* g, const Derived& d, int32_t evict_first_frame, int32_t q0) {
   if (g->reindex_mode == 1 || g->n_temporal_pairs == 0) return true;
   const double span_end = g->g_mode == 0 ? g->g_span_S : g->g_recent_R + g->g_span_S;
@@ -309,7 +314,8 @@ dcp_status paged_view(const dcp_paged_cache* c, const dcp_config* g, dcp_cache* 
 dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dcp_config* cfg, const float* x0hat,
                            const float* xref, int32_t dd, int32_t evict_slot, int32_t evict_first_frame,
                            int32_t q0_prev, int32_t q0, const uint8_t* head_is_static, int32_t* kept_dev,
-                           int32_t* kept_host_pinned, void* ws, size_t ws_bytes, void* stream);
+                           int32_t* kept_host_pinned, void* ws, size_t ws_bytes, void* stream,
+                           size_t ws_clear_bytes = 0);
 
 // Read-time re-index: the scan kernel's table CTAs build the turn t -> t~(t; q0) for frames [T_s, q0) and its plane
 // checks find the longest history; the read kernel follows on the stream.
@@ -399,6 +405,14 @@ SnapParams snap_params(const dcp_cache* c, const dcp_config* g, const Derived& d
 }  // namespace
 
 namespace dcp {
+dcp_status prune_step_cleared(const dcp_cache* cache, const dcp_config* cfg, const float* x0hat, const float* xref,
+                              int32_t dd, int32_t evict_slot, int32_t evict_first_frame, int32_t q0_prev, int32_t q0,
+                              const uint8_t* head_is_static, int32_t* kept_dev, int32_t* kept_host_pinned, void* ws,
+                              size_t ws_bytes, size_t ws_clear_bytes, void* stream) {
+  return prune_step_impl(cache, nullptr, cfg, x0hat, xref, dd, evict_slot, evict_first_frame, q0_prev, q0,
+                         head_is_static, kept_dev, kept_host_pinned, ws, ws_bytes, stream, ws_clear_bytes);
+}
+
 int sm_count() {
   static std::atomic<int> cache[kMaxDevices];  // zero until first read on that device
   int dev = 0;
@@ -590,10 +604,13 @@ dcp_status dcp_paged_read_history_keys(const dcp_paged_cache* cache, const dcp_c
 
 namespace {
 
+// ws_clear_bytes > 0: the first ws_clear_bytes of the workspace are zeroed on the stream after every host check has
+// passed and before the first kernel (a workspace shared by every call, whose start must be zero).
 dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dcp_config* cfg, const float* x0hat,
                            const float* xref, int32_t dd, int32_t evict_slot, int32_t evict_first_frame,
                            int32_t q0_prev, int32_t q0, const uint8_t* head_is_static, int32_t* kept_dev,
-                           int32_t* kept_host_pinned, void* ws, size_t ws_bytes, void* stream) {
+                           int32_t* kept_host_pinned, void* ws, size_t ws_bytes, void* stream,
+                           size_t ws_clear_bytes) {
   Derived d;
   if (check_cache_cfg(cache, cfg, &d) != DCP_OK) return DCP_EINVAL;
   if (check_eviction(cfg, d, evict_slot, evict_first_frame, q0) != DCP_OK) return DCP_EINVAL;
@@ -657,6 +674,7 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
     sp.n_blocks = pv->n_blocks;
     sp.n_tbl_slices = (sp.n_tbl_a + sp.n_tbl_b + kThreads - 1) / kThreads;
   }
+  if (ws_clear_bytes && cudaMemsetAsync(ws, 0, ws_clear_bytes, st) != cudaSuccess) return DCP_ECUDA;
   // scan -> re-index (reads the history lengths before the step) -> gather (grows them)
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;

@@ -236,6 +236,12 @@ cudaError_t launch_snapshot(const SnapParams& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch, bool paged);
 cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch, bool paged);
 int sm_count();
+// dcp_prune_step that first zeroes ws[0, ws_clear_bytes) on the stream, once every host check has passed (nothing is
+// launched for a refused call).
+dcp_status prune_step_cleared(const dcp_cache* cache, const dcp_config* cfg, const float* x0hat, const float* xref,
+                              int32_t dd, int32_t evict_slot, int32_t evict_first_frame, int32_t q0_prev, int32_t q0,
+                              const uint8_t* head_is_static, int32_t* kept_dev, int32_t* kept_host_pinned, void* ws,
+                              size_t ws_bytes, size_t ws_clear_bytes, void* stream);
 
 // Per-device launch set-up of one kernel, made on first use on each device: the dynamic shared-memory opt-in (a
 // per-device function attribute) and the number of CTAs that fit on an SM with that much shared memory.  Host

@@ -8,30 +8,78 @@
 // DCP_NOALLOC_WORKSPACE_BYTES; a cache and config whose workspace (dcp_workspace_size) is larger are rejected.
 //
 // In host code the array's name is only a host-side stand-in, not a device address, so its device address is
-// looked up once per device (cudaGetSymbolAddress, with that device current) on the first call made with that
-// device current, and passed to the kernels.  Make that first call before any stream capture.
+// looked up (cudaGetSymbolAddress) on the first call made in each CUDA context (one per device for the runtime's
+// primary contexts), with that context current, and passed to the kernels.  Make that first call before any stream
+// capture.  The lookup is remembered per context id, so a context created later (after cudaDeviceReset, say) gets a
+// lookup of its own instead of a stale address.
 //
-// Every call shares the one array and leaves its contents behind; the parts that must start at zero (the scan's
-// control block and its look-back tile states) are cleared on the stream at the start of each call.  Calls whose
-// work overlaps on the GPU (different streams, or different threads on one device) race on the array: order them.
+// Every call shares the one array and leaves its contents behind.  The part that must start at zero, the scan's
+// 256-byte control block (its completion counter and the atomically folded plane checks), is cleared on the stream
+// once the call's arguments have passed every host check, right before its first kernel; a refused call launches
+// nothing.  Calls whose work overlaps on the GPU (different streams, or different threads on one device) race on the
+// array: order them.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "dcp_internal.cuh"
 
 namespace {
 
 __device__ __align__(256) unsigned char g_noalloc_ws[DCP_NOALLOC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_noalloc_addr[kMaxDevices] = {nullptr};
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+constexpr int kMaxContexts = 64;
+struct AddressCache {
+  std::mutex m;
+  bool resolved = false;
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+  int n = 0;
+  unsigned long long ctx_id[kMaxContexts];
+  void* addr[kMaxContexts];
+};
+AddressCache g_cache;
+
+// The id of the calling thread's current context (the driver's own unique id for the process lifetime), or 0 when
+// the thread has no current context yet.  The driver entry points come through the runtime, so the library does not
+// link the driver library itself.
+bool current_context_id(AddressCache& c, unsigned long long* id) {
+  if (!c.resolved) {
+    void *f1 = nullptr, *f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1{}, q2{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+      return false;
+    c.get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+    c.get_id = reinterpret_cast<CtxGetIdFn>(f2);
+    c.resolved = true;
+  }
+  CUcontext ctx = nullptr;
+  if (c.get_current(&ctx) != CUDA_SUCCESS) return false;
+  *id = 0;
+  return ctx == nullptr || c.get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 dcp_status noalloc_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DCP_ECUDA;
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess || p == nullptr) return DCP_ECUDA;
-    g_noalloc_addr[dev] = p;
-  }
-  *out = g_noalloc_addr[dev];
+  std::lock_guard<std::mutex> guard(g_cache.m);
+  unsigned long long id = 0;
+  if (!current_context_id(g_cache, &id)) return DCP_ECUDA;
+  for (int i = 0; id && i < g_cache.n; ++i)
+    if (g_cache.ctx_id[i] == id) {
+      *out = g_cache.addr[i];
+      return DCP_OK;
+    }
+  void* p = nullptr;  // the lookup makes the device's primary context current when the thread had none
+  if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess || p == nullptr) return DCP_ECUDA;
+  if (!current_context_id(g_cache, &id) || id == 0) return DCP_ECUDA;
+  const int slot = g_cache.n < kMaxContexts ? g_cache.n++ : (int)(id % kMaxContexts);
+  g_cache.ctx_id[slot] = id;
+  g_cache.addr[slot] = p;
+  *out = p;
   return DCP_OK;
 }
 
@@ -47,11 +95,7 @@ extern "C" dcp_status dcp_prune_step_noalloc(const dcp_cache* cache, const dcp_c
   void* ws = nullptr;
   const dcp_status rc = noalloc_address(&ws);
   if (rc != DCP_OK) return rc;
-  const int64_t C = (int64_t)cfg->tokens_per_frame * cfg->frames_per_chunk;
-  const dcp::Layout lay = dcp::make_layout(C, (int64_t)cache->L * cache->H, cfg->frames_per_chunk,
-                                           cfg->n_temporal_pairs, cfg->max_frames);
-  if (cudaMemsetAsync(ws, 0, lay.ell, (cudaStream_t)stream) != cudaSuccess) return DCP_ECUDA;
-  return dcp_prune_step(cache, cfg, x0hat_dev, xref_dev, d, evict_slot, evict_first_frame, q0_prev, q0,
-                        head_is_static_dev, kept_dev, kept_host_pinned, ws, (size_t)DCP_NOALLOC_WORKSPACE_BYTES,
-                        stream);
+  return dcp::prune_step_cleared(cache, cfg, x0hat_dev, xref_dev, d, evict_slot, evict_first_frame, q0_prev, q0,
+                                 head_is_static_dev, kept_dev, kept_host_pinned, ws,
+                                 (size_t)DCP_NOALLOC_WORKSPACE_BYTES, sizeof(dcp::Ctrl), stream);
 }

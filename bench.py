@@ -34,8 +34,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-# DRAM bytes (read + write) of one full-depth gather launch (gather_staged_kernel) from the ncu capture summarised in
-# profiles/gather_kernel_full_depth_dram.md.  They describe the kernel sources they were taken on: when the hash of
+# DRAM bytes (read + write) of one full-depth gather launch, from an ncu capture of dram__bytes_read.sum and
+# dram__bytes_write.sum on the same kernel.  They describe the kernel sources they were taken on: when the hash of
 # those sources differs, the bench reports no traffic figure.
 GATHER_TRAFFIC_BYTES = 1_503_282_432
 GATHER_TRAFFIC_SOURCES_SHA256 = "7a70e3aec16efe017e28ea5a7379fa510deefd84d5e8a0ad0270183ab437f884"
@@ -910,6 +910,74 @@ class OracleSample:
                 f"one thread")
 
 
+# ------------------------------------------------------------------------------------------ the JSON line
+L2_NOTE = "flushed between GPU steps (256 MB write, then 256 MB read to drain dirty lines); cache 30.7 GB >> L2"
+COMPUTE_NOTE = "fp32 score, fp32 compensated rotation, bf16 storage (the CPU oracle: fp64, rounded once to bf16)"
+
+
+def line_config(w, k: int) -> dict:
+    """The `config` object of the JSON line, the same for the GPU arm and the reference (CPU oracle) arm: the workload
+    and its step's kept count and algorithmic bytes (history empty: nothing is re-indexed)."""
+    return {"workload": w.name, "L": w.L, "H": w.H, "D": w.D, "tokens_per_chunk": w.C, "d": w.d, "kept": k,
+            "evicting_chunk": w.evictions()[-1][0], "q0": w.evictions()[-1][2],
+            "algorithmic_bytes_per_step": w.algorithmic_bytes(k, w.n_planes, 0), "l2": L2_NOTE}
+
+
+def _rate(us: float, nbytes: int, peak: float) -> dict:
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_step": round(us, 1), "GB_per_s": round(gbs) if gbs >= 100 else round(gbs, 2),
+            "frac": round(gbs / peak, 3) if gbs >= 100 else round(gbs / peak, 5)}
+
+
+def compact_extra(d: dict, peak: float) -> dict:
+    """Every extra workload as a short {us_per_step, GB_per_s, frac} object (frac of the measured copy peak), so that
+    the whole summary sits in the last part of the line."""
+    out = {}
+
+    def put(name, src, us_key="us_per_step", bytes_key=None):
+        if src is None:
+            return
+        nbytes = src[bytes_key] if bytes_key else src["GB_per_s"] * 1e9 * src[us_key] * 1e-6
+        out[name] = _rate(src[us_key], nbytes, peak)
+    put("full_rotated_2r", d.get("full_depth_rotated"))
+    if "full_depth_rotated" in d:
+        out["full_rotated_2r"]["gather_us"] = round(d["full_depth_rotated"]["gather_us"], 1)
+    put("random_ablation", d.get("full_depth_random_ablation"))
+    put("paged_hnd", d.get("full_depth_paged_hnd"))
+    put("paged_nhd", d.get("full_depth_paged_nhd"))
+    put("paged_hnd_2r", d.get("full_depth_rotated_paged_hnd"))
+    put("tiny_fp32", d.get("tiny_fp32_single_prune"), bytes_key="algorithmic_bytes")
+    put("mid_bf16", d.get("mid_bf16_single_eviction"), bytes_key="algorithmic_bytes")
+    hs = d.get("head_specialised_prefix")
+    if hs:
+        for i, e in enumerate(hs["evictions"]):
+            put(f"hs_prefix_ev{i + 1}", e)
+    for name, key in (("rollout_eager", "minute_rollout_gqa8"),
+                      ("rollout_read_time", "minute_rollout_gqa8_read_time_reindex")):
+        r = d.get(key)
+        if r:
+            gbs = r["GB_per_s"]
+            out[name] = {"us_per_step": round(r["mean_us_per_step"], 1), "GB_per_s": round(gbs),
+                         "frac": round(gbs / peak, 3), "last10_us": round(r["last10_mean_us"], 1),
+                         "PR": round(r["cumulative_PR"], 4)}
+            if "read_history_keys" in r:
+                rh = r["read_history_keys"]
+                out["read_final_history"] = _rate(rh["us"], rh["bytes"], peak)
+            if "drift_eager_vs_read_time" in r:
+                out[name]["drift_of_pair"] = round(r["drift_eager_vs_read_time"]["max_of_pair_length"], 4)
+    g = d.get("cuda_graph_replay")
+    if g:
+        out["graph_replay_us"] = {x["workload"].split("_")[0]: [round(x["direct_us"], 1), round(x["graph_replay_us"], 1)]
+                                  for x in g}
+    sn = d.get("host_snapshot_restore")
+    if sn:
+        out["host_snapshot"] = {"GB_per_s": round(sn["snapshot_GB_per_s"], 1),
+                                "frac_of_link": round(sn["frac_of_plain_copy"]["snapshot"], 3)}
+        out["host_restore"] = {"GB_per_s": round(sn["restore_GB_per_s"], 1),
+                               "frac_of_link": round(sn["frac_of_plain_copy"]["restore"], 3)}
+    return out
+
+
 # ------------------------------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -924,6 +992,8 @@ def main():
     ap.add_argument("--tokens-per-frame", type=int, default=0,
                     help="profiling captures only: the same workload with shorter chunks (every plane kept, a few GB)")
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before the timed region")
+    ap.add_argument("--detail", default="", help="write the full result of every extra workload (curves, per-kernel "
+                                                 "times) as JSON to this file; the line carries a compact summary")
     ap.add_argument("--case", default="step",
                     choices=["step", "reindex", "score", "random", "read", "snapshot", "paged-hnd", "paged-nhd"],
                     help="step: the prune step (default); reindex: dcp_rope_reindex of a 64-plane cache with 90,000 "
@@ -971,8 +1041,11 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        import __graft_entry__
-        __graft_entry__.build()
+        # the CPU oracle and the input generator only: the product library is neither built nor loaded here
+        import oracle
+        import synth
+        oracle.build()
+        synth.build()
         sample = OracleSample(w, args.oracle_planes)
         for _ in range(args.warmup):
             sample.step()
@@ -982,8 +1055,7 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(secs)) * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                "data": "synthetic", "config": {"workload": w.name, "L": w.L, "H": w.H, "D": w.D,
-                                                "tokens_per_chunk": w.C, "d": w.d},
+                "data": "synthetic", "config": line_config(w, sample.k), "compute": COMPUTE_NOTE,
                 "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
                 "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -1049,11 +1121,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms_max"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "L": w.L, "H": w.H, "D": w.D, "tokens_per_chunk": w.C, "d": w.d,
-                   "kept": res["k"], "evicting_chunk": w.evictions()[-1][0], "q0": w.evictions()[-1][2],
-                   "algorithmic_bytes_per_step": res["alg_bytes"],
-                   "l2": "flushed between steps (256 MB write, then 256 MB read to drain dirty lines)",
-                   "compute": "fp32 score, fp32 compensated rotation, bf16 storage"},
+        "config": line_config(w, res["k"]), "compute": COMPUTE_NOTE,
         "us_per_step": res["ms_max"] * 1e3,
         "pct_of_nominal_hbm": 100.0 * (value / world) / NOMINAL_HBM_GBS,
         "pct_of_measured_hbm": 100.0 * (value / world) / peak,
@@ -1075,8 +1143,6 @@ def main():
                                  "written to page-locked host memory by the scan kernel",
                        "with_explicit_copies": {"median_us_per_step": res["copy_e2e_ms"] * 1e3,
                                                 "h2d_copy_us_median": res["h2d_ms"] * 1e3}}
-    if extra:
-        line["extra"] = extra
     if not args.no_extra:
         sample = OracleSample(w, args.oracle_planes)
         sample.step()
@@ -1084,6 +1150,11 @@ def main():
         line["cpu_baseline"] = {"value": sample.bytes_per_step() / float(np.mean(secs)) / 1e9, "unit": "GB/s",
                                 "cores": 1, "kind": "oracle", "sample": sample.describe(5),
                                 "host_cores_available": cores, "host_cpu": _cpu_model()}
+    if extra:
+        if args.detail:
+            with open(args.detail, "w") as f:
+                json.dump(extra, f)
+        line["extra"] = compact_extra(extra, peak)  # last: the end of the line holds every workload's summary
     print(json.dumps(line))
 
 

@@ -186,10 +186,14 @@ dcp_status dcp_prune_step(const dcp_cache* cache, const dcp_config* cfg, const f
  * allocating routine.
  *   - Returns DCP_EINVAL when dcp_workspace_size(cache, cfg) is 0 (invalid) or larger than the scratch array, and
  *     for every argument dcp_prune_step rejects.
- *   - The first call made with a given device current looks up the array's device address (cudaGetSymbolAddress)
- *     for that device; make that first call before any stream capture.
- *   - Every call shares the one array.  The parts that must start at zero are cleared on `stream` at the start of
- *     each call; calls whose work overlaps on the GPU (other streams or threads on the same device) race on it. */
+ *   - The first call made in a CUDA context (for the runtime's primary contexts: the first call with a given device
+ *     current) looks up the array's device address in that context (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.  The address is remembered per context id, so a context created later (after
+ *     cudaDeviceReset, say) is looked up afresh.
+ *   - Every call shares the one array and finds the previous call's contents in it.  Only the scan's 256-byte control
+ *     block must start at zero: it is cleared on `stream` once the arguments have passed every host check, right
+ *     before the first kernel (a refused call launches nothing).  Calls whose work overlaps on the GPU (other streams
+ *     or threads on the same device) race on the array: order them. */
 dcp_status dcp_prune_step_noalloc(const dcp_cache* cache, const dcp_config* cfg, const float* x0hat_dev,
                                   const float* xref_dev, int32_t d, int32_t evict_slot, int32_t evict_first_frame,
                                   int32_t q0_prev, int32_t q0, const uint8_t* head_is_static_dev, int32_t* kept_dev,

@@ -12,7 +12,8 @@ Wide draws (1024 to 1600 planes, rows of at most 288 bytes, short chunks) run st
 shared-memory staged gather, across row sizes and dtypes, and steps that turn on the register-staged gather; some of
 them run on paged pools (HND or NHD, 8 to 32 positions per block), which take the register-staged gather.  Big
 draws use rows of 1 to 4 KiB (the largest the library takes) with up to 1024 temporal pairs; edge draws use chunks of
-1 to 33 tokens and score rows of 1 to 64 values.
+1 to 33 tokens and score rows of 1 to 64 values.  Boundary draws put the last eviction exactly on the edge of g's
+identity on the leaving chunk (where the library skips the chunk's turn) and one frame past it, for both maps g.
 """
 import numpy as np
 import pytest
@@ -159,14 +160,52 @@ def draw_edge(case: int):
 
 N_EDGE = len(EDGE)
 
+# the host's no-turn decision (g is the identity on the leaving chunk's offsets): draws on both sides of each boundary
+# (g mode, boundary, side); the chunk's oldest offset q0 - evict_first_frame is (w + 1) F for every eviction
+BOUNDARY = [(m, b, side) for m in (0, 1) for b in ("recent", "span") for side in ("at", "past")]
+
+
+def draw_boundary(case: int):
+    """A 1024-plane cache (rows of 128 bytes, 8-token chunks) whose last eviction sits exactly on a boundary of g's
+    identity or one frame past it: q0 - evict_first_frame in {R, R + 1} while g compresses, or q0 - T_s in
+    {span end, span end + 1} while the chunk's oldest offset is past R.  On the "at" side no kept key turns (the staged
+    gather, no cos/sin table for the chunk); one frame past it the oldest frame's keys turn (the register-staged
+    gather)."""
+    mode, bound, side = BOUNDARY[case]
+    F, T, sink, win, n_ev = 2, 4, 1, 2, 3
+    last = sink + n_ev - 1
+    q0 = (last + win + 1) * F
+    oldest, dmax = (win + 1) * F, q0 - sink * F          # 6 and 10
+    if bound == "recent":
+        R = oldest if side == "at" else oldest - 1        # offset = R, or R + 1
+        S = R if mode == 0 else 1                         # span end R or R + 1: below dmax, so g compresses
+    else:
+        R = win * F                                       # 4 < oldest: the oldest frame lies in g's linear part
+        end = dmax if side == "at" else dmax - 1
+        S = end if mode == 0 else end - R
+    w = scaled(TINY, name=f"sweep_boundary_{case}", index=500 + case, L=32, H=32, D=64, dtype=0,
+               n_temporal_pairs=int(np.random.default_rng(0xB0D + case).integers(1, 33)), tokens_per_frame=T,
+               frames_per_chunk=F, d=16, sink_chunks=sink, window_chunks=win, R=float(R), S=float(S), g_mode=mode,
+               hist_cap=n_ev * T * F, max_frames=q0 + 2 * F, evict_chunk=last,
+               history_chunks=tuple(range(sink, last)), seed=9700 + case)
+    while not _clear_of_tie_band(w) or not np.any(oracle.score(*w.score_inputs(last)) > np.float32(w.gamma)):
+        w = scaled(w, seed=w.seed + 100)  # scores clear of gamma, and at least one kept token at the last eviction
+    return w, {"keep_rule": 0, "random_seed": 0, "reindex_mode": 0}, None, None
+
+
+N_BOUNDARY = len(BOUNDARY)
+
 
 @pytest.mark.parametrize("case", [("narrow", i) for i in range(N_CASES)] + [("wide", i) for i in range(N_WIDE)] +
-                         [("big", i) for i in range(N_BIG)] + [("edge", i) for i in range(N_EDGE)],
+                         [("big", i) for i in range(N_BIG)] + [("edge", i) for i in range(N_EDGE)] +
+                         [("boundary", i) for i in range(N_BOUNDARY)],
                          ids=[f"case{i}" for i in range(N_CASES)] + [f"wide{i}" for i in range(N_WIDE)] +
-                         [f"big{i}" for i in range(N_BIG)] + [f"edge{i}" for i in range(N_EDGE)])
+                         [f"big{i}" for i in range(N_BIG)] + [f"edge{i}" for i in range(N_EDGE)] +
+                         [f"boundary_m{m}_{b}_{sd}" for m, b, sd in BOUNDARY])
 def test_sweep_case(gpu, case):
     kind, case = case
-    w, over, hsm, paged = {"narrow": draw, "wide": draw_wide, "big": draw_big, "edge": draw_edge}[kind](case)
+    w, over, hsm, paged = {"narrow": draw, "wide": draw_wide, "big": draw_big, "edge": draw_edge,
+                           "boundary": draw_boundary}[kind](case)
     ocfg = replay.cfg_of(w)
     for key, val in over.items():
         setattr(ocfg, key, val)

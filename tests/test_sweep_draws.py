@@ -3,7 +3,9 @@ schedule replays in the oracle with every step accepted, and the draws reach the
 import numpy as np
 
 from oracle import replay
-from tests.test_gpu_sweep import N_BIG, N_CASES, N_EDGE, N_WIDE, draw, draw_big, draw_edge, draw_wide
+import oracle
+from tests.test_gpu_sweep import (BOUNDARY, N_BIG, N_BOUNDARY, N_CASES, N_EDGE, N_WIDE, draw, draw_big, draw_boundary,
+                                  draw_edge, draw_wide)
 
 
 def test_sweep_draws_replay_in_the_oracle():
@@ -79,3 +81,28 @@ def test_edge_draws_replay_in_the_oracle():
             setattr(cfg, key, val)
         hc = replay.new_host_cache(w)
         replay.replay(w, hc, w.evictions(), hsm, cfg=cfg)
+
+
+def test_boundary_draws_turn_exactly_past_the_boundary():
+    """On the "at" side of each boundary the oracle's last eviction moves every kept key row bitwise (g is the
+    identity on the chunk); one frame past it some kept key turns.  The GPU sweep compares both with the oracle, so a
+    no-turn decision taken on the wrong side fails there."""
+    for case in range(N_BOUNDARY):
+        w, over, hsm, _ = draw_boundary(case)
+        _, _, side = BOUNDARY[case]
+        assert w.n_planes >= 1024 and w.D * w.esize <= 288
+        hc, (c, q0_prev, q0) = replay.state_before_last(w)
+        T_s = w.sink_chunks * w.F
+        end = w.S if w.g_mode == 0 else w.R + w.S
+        if BOUNDARY[case][1] == "recent":
+            assert q0 - w.first_frame(c) == (w.R if side == "at" else w.R + 1) and q0 - T_s > end
+        else:
+            assert q0 - T_s == (end if side == "at" else end + 1) and q0 - w.first_frame(c) > w.R
+        src = hc.k[:, :, w.win_row0 + w.slot_of(c) * w.C: w.win_row0 + (w.slot_of(c) + 1) * w.C].copy()
+        common = int(hc.hist_len[0])
+        rc, _, _, idx = oracle.prune_step(hc, replay.cfg_of(w), *w.score_inputs(c), w.slot_of(c), w.first_frame(c),
+                                          q0_prev, q0)
+        assert rc == oracle.OK and len(idx) > 0
+        moved = hc.k[:, :, w.sink_rows + common: w.sink_rows + common + len(idx)]
+        same = np.array_equal(moved, src[:, :, idx])
+        assert same == (side == "at"), (case, BOUNDARY[case])
