@@ -16,7 +16,8 @@ FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std
 
 def _deps():
     out = [os.path.join(CSRC, s) for s in SOURCES]
-    out += [os.path.join(CSRC, "dcp_internal.cuh"), os.path.join(HERE, "..", "include", "dcp.h")]
+    out += [os.path.join(CSRC, h) for h in ("dcp_internal.cuh", "rephase_body.cuh")]
+    out += [os.path.join(HERE, "..", "include", "dcp.h")]
     return out
 
 

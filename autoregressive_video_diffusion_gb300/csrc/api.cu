@@ -165,7 +165,7 @@ GatherParams gather_params(const dcp_cache* c, const dcp_config* g, const Derive
   gp.n_t = g->n_temporal_pairs;
   gp.dtype = c->dtype;
   gp.n_frames = g->frames_per_chunk;
-  gp.no_turn = 0;  // set by the callers that know q0
+  gp.no_turn = 0;  // set by the callers that know q0 (set_turn)
   gp.status = c->status;
   return gp;
 }
@@ -208,6 +208,14 @@ bool chunk_keeps_phase(const dcp_config* g, const Derived& d, int32_t evict_firs
   if (g->reindex_mode == 1 || g->n_temporal_pairs == 0) return true;
   const double span_end = g->g_mode == 0 ? g->g_span_S : g->g_recent_R + g->g_span_S;
   return (double)(q0 - d.T_s) <= span_end || (double)(q0 - evict_first_frame) <= g->g_recent_R;
+}
+
+// The turn of the leaving chunk's keys for a gather at q0: none (no_turn: the scan builds no table for the chunk), or
+// the scan's table CTAs build it.
+void set_turn(GatherParams& gp, ScanParams& sp, const dcp_config* g, const Derived& d, int32_t evict_first_frame,
+              int32_t q0) {
+  gp.no_turn = chunk_keeps_phase(g, d, evict_first_frame, q0) ? 1 : 0;
+  sp.g_frames = gp.no_turn ? 0 : g->frames_per_chunk;
 }
 
 // ------------------------------------------------------------------------------------------ snapshot helpers
@@ -503,17 +511,14 @@ dcp_status dcp_compact_layers(const dcp_cache* cache, const dcp_config* cfg, int
   sp.update_cache = 1;
   sp.head_is_static = head_is_static;
   sp.evict_first_frame = evict_first_frame;
-  sp.g_frames = cfg->frames_per_chunk;
   sp.q0 = q0;
   sp.q0_prev = q0;
-  const bool no_turn = chunk_keeps_phase(cfg, d, evict_first_frame, q0);
-  if (no_turn) sp.g_frames = 0;  // no table for the leaving chunk: its keys move unturned
+  GatherParams gp = gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame);
+  set_turn(gp, sp, cfg, d, evict_first_frame, q0);
   if (head_is_static) sp.dyn_list = at<int32_t>(ws, d.lay.dyn);  // the scan lists the receiving planes
   finish_tables(sp);
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
-  GatherParams gp = gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame);
-  gp.no_turn = no_turn ? 1 : 0;
   if (head_is_static) gp.dyn_list = at<int32_t>(ws, d.lay.dyn);
   return cuda_ok(launch_gather(gp, st, true, false));
 }
@@ -647,14 +652,12 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
   sp.head_is_static = head_is_static;
   sp.evict_first_frame = evict_first_frame;
   sp.random_stream = ((uint64_t)cfg->random_seed << 32) | (uint32_t)evict_first_frame;
-  sp.g_frames = cfg->frames_per_chunk;
   sp.h_lo = d.T_s;
   sp.h_hi = rephase ? evict_first_frame : d.T_s;
   sp.q0 = q0;
   sp.q0_prev = q0_prev;
   GatherParams gp = gather_params(cache, cfg, d, ws, evict_slot, head_is_static, evict_first_frame);
-  gp.no_turn = chunk_keeps_phase(cfg, d, evict_first_frame, q0) ? 1 : 0;
-  if (gp.no_turn) sp.g_frames = 0;  // no table for the leaving chunk: its keys move unturned
+  set_turn(gp, sp, cfg, d, evict_first_frame, q0);
   if (head_is_static) {  // the scan lists the receiving planes; the gather splits that list only
     sp.dyn_list = at<int32_t>(ws, d.lay.dyn);
     gp.dyn_list = sp.dyn_list;
@@ -675,15 +678,21 @@ dcp_status prune_step_impl(const dcp_cache* cache, const PagedView* pv, const dc
     sp.n_tbl_slices = (sp.n_tbl_a + sp.n_tbl_b + kThreads - 1) / kThreads;
   }
   if (ws_clear_bytes && cudaMemsetAsync(ws, 0, ws_clear_bytes, st) != cudaSuccess) return DCP_ECUDA;
-  // scan -> re-index (reads the history lengths before the step) -> gather (grows them)
+  // scan -> re-index (reads the history lengths before the step) -> gather (grows them); when every plane receives,
+  // the re-index and the gather run as one launch (their rows are disjoint, and every length before the step is the
+  // scan's common length)
   dcp_status rc = cuda_ok(launch_scan(sp, st));
   if (rc != DCP_OK) return rc;
-  if (rephase) {
+  const bool fused = rephase && !head_is_static;
+  if (rephase && !fused) {
     rc = cuda_ok(launch_rephase(rp, st, true, pv != nullptr));
     if (rc != DCP_OK) return rc;
   }
   if (g_ev_after_scan && cudaEventRecord(g_ev_after_scan, st) != cudaSuccess) return DCP_ECUDA;
-  rc = cuda_ok(launch_gather(gp, st, g_ev_after_scan == nullptr, pv != nullptr));
+  if (fused)
+    rc = cuda_ok(launch_step_fused(gp, rp, st, g_ev_after_scan == nullptr, pv != nullptr));
+  else
+    rc = cuda_ok(launch_gather(gp, st, g_ev_after_scan == nullptr, pv != nullptr));
   if (rc != DCP_OK) return rc;
   if (g_ev_after_gather && cudaEventRecord(g_ev_after_gather, st) != cudaSuccess) return DCP_ECUDA;
   return rc;

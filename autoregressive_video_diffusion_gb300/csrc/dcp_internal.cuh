@@ -115,6 +115,7 @@ struct ScanParams {
   int32_t g_mode;
   int32_t T_s;             // first non-sink frame
   int32_t q0, q0_prev;
+  int32_t n_counted;       // CTAs that take part in the completion count (set by launch_scan)
 };
 
 // Table entries per table CTA: at most kTableEntries, at least kTableMinEntries, spread over about
@@ -235,6 +236,9 @@ cudaError_t launch_read(const ReadParams& p, cudaStream_t s, bool paged);
 cudaError_t launch_snapshot(const SnapParams& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch, bool paged);
 cudaError_t launch_rephase(const RephaseParams& p, cudaStream_t s, bool overlap_launch, bool paged);
+// The re-index and the gather of a step in one launch (every plane receives: no static heads; gp.vb == rp.vb).
+cudaError_t launch_step_fused(const GatherParams& gp, const RephaseParams& rp, cudaStream_t s, bool overlap_launch,
+                              bool paged);
 int sm_count();
 // dcp_prune_step that first zeroes ws[0, ws_clear_bytes) on the stream, once every host check has passed (nothing is
 // launched for a refused call).
@@ -304,6 +308,20 @@ __device__ __forceinline__ float4 dev_trig_entry(double phi) {
   const float chi = round_to_16_bits(c), shi = round_to_16_bits(s);
   return make_float4(chi, __double2float_rn(__dsub_rn(c, (double)chi)), shi,
                      __double2float_rn(__dsub_rn(s, (double)shi)));
+}
+
+// Table entry of the turn from frame t to t~(t; q0) for rotary pair pp, with theta_pp = base^(-pp / n_t) evaluated as
+// exp2(log2(base) * (-pp / n_t)) (the same value to a few ulps of fp64, far below the 2^-40 the entry carries, and
+// much cheaper than pow on a part with a low fp64 rate); *moves: t~ differs from t.  Every table of the library is
+// built by this function, so tables built by different kernels hold the same bits.  (Each gather CTA building the
+// leaving chunk's table itself, before its wait for the scan, measured slower: 304 CTAs paying GB300's low fp64 rate
+// for the same 88 entries made the rotated full-depth gather 248 instead of 238 us.)
+__device__ __forceinline__ float4 dev_turn_entry(double t, int pp, int n_t, double log2_base, double q0, double T_s,
+                                                 double R, double S, int mode, bool identity, bool* moves) {
+  const double delta = identity ? 0.0 : __dsub_rn(dev_phase(t, q0, T_s, R, S, mode), t);
+  const double theta = exp2(__dmul_rn(-(double)pp / (double)n_t, log2_base));
+  *moves = delta != 0.0;
+  return dev_trig_entry(__dmul_rn(theta, delta));
 }
 
 // Rotate one pair (a, b) of fp32 values by the angle whose cos/sin pairs are in t:

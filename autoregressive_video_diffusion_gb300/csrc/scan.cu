@@ -14,10 +14,13 @@
 //                (receiving planes' shortest and longest history, lowest receiving plane, longest history) and, for
 //                paged caches, checks 256 block-table entries.  They have CTAs of their own so that no tile starts
 //                late (measured: the tiles that also ran the checks finished 0.9 us later).
-//   final CTA    the last CTA to finish (completion counter) turns the ballot words into the ordered index list
-//                with one block-wide exclusive scan of their popcounts per 256 words, decides capacity and
-//                consistency, publishes the verdict for the kernels that follow and resets the counters.  Under
-//                the Random ablation (keep rule 2) it first draws the kept set (radix select, below).
+//   final CTA    the last tile or check CTA to finish (completion counter) turns the ballot words into the ordered
+//                index list with one block-wide exclusive scan of their popcounts per 256 words, decides capacity
+//                and consistency, publishes the verdict for the kernels that follow and resets the counters.  Under
+//                the Random ablation (keep rule 2) it first draws the kept set (radix select, below).  The table
+//                CTAs, whose fp64 chains are the slowest part of the kernel, take no part in the count: nothing in
+//                the final CTA reads the tables, and the kernels that do wait for the whole grid, so the compaction
+//                runs while the tables are still being built instead of after them.
 // Every step of that chain is a fixed number of dependent memory round trips; no CTA waits on another.  (A
 // decoupled look-back over 98 tiles measured 11.8 us for a 6240-token chunk on GB300, where each polling round is a
 // cross-die L2 round trip; this single-pass form removes the polling.)  The kernel lets its dependents launch early
@@ -179,8 +182,7 @@ __device__ void table_checks(const ScanParams& p, int slice) {
   if ((threadIdx.x & 31) == 0 && bad) atomicMax(&p.ctrl->acc_bad, 1);
 }
 
-// theta_p = base^(-p / n_t) is evaluated as exp2(log2(base) * (-p / n_t)): the same value to a few ulps of fp64,
-// far below the 2^-48 carried by the table, and much cheaper than pow on a part with a low fp64 rate.
+// theta_p = base^(-p / n_t) is evaluated as exp2(log2(base) * (-p / n_t)) (dev_turn_entry).
 __device__ void table_work(const ScanParams& p, int block) {
   if (threadIdx.x >= p.tbl_per) return;
   const double log2_base = log2(p.base);
@@ -189,12 +191,10 @@ __device__ void table_work(const ScanParams& p, int block) {
   const int n_h = (p.h_hi - p.h_lo) * p.n_t;
   if (e < n_g) {
     const int f = e / p.n_t, pp = e - f * p.n_t;
-    const double t = (double)(p.evict_first_frame + f);
-    const double delta =
-        p.g_identity ? 0.0 : __dsub_rn(dev_phase(t, (double)p.q0, (double)p.T_s, p.R, p.S, p.g_mode), t);
-    const double theta = exp2(__dmul_rn(-(double)pp / (double)p.n_t, log2_base));
-    p.trig_g[e] = dev_trig_entry(__dmul_rn(theta, delta));
-    if (pp == 0) p.rot_g[f] = delta != 0.0;
+    bool moves = false;
+    p.trig_g[e] = dev_turn_entry((double)(p.evict_first_frame + f), pp, p.n_t, log2_base, (double)p.q0,
+                                 (double)p.T_s, p.R, p.S, p.g_mode, p.g_identity != 0, &moves);
+    if (pp == 0) p.rot_g[f] = moves ? 1 : 0;
   } else if (e - n_g < n_h) {
     const int e2 = e - n_g;
     const int f = e2 / p.n_t, pp = e2 - f * p.n_t;
@@ -369,8 +369,12 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanParams p) {
   allow_dependents();
   const int id = blockIdx.x;
   const int check0 = p.n_tiles + p.n_trig_blocks;  // the check CTAs follow the tile and table CTAs
-  if (id < p.n_tiles) tile_work(p, id, s_ell);
-  else if (id < check0) table_work(p, id - p.n_tiles);
+  if (id < p.n_tiles) {
+    tile_work(p, id, s_ell);
+  } else if (id < check0) {
+    table_work(p, id - p.n_tiles);
+    if (p.n_counted < (int)gridDim.x) return;  // not counted: the tables are read by the later kernels only
+  }
   if (id >= check0 && id - check0 < p.n_plane_slices) plane_checks(p, id - check0, s_warp, &s_last);
   if (id >= check0 && id - check0 < p.n_tbl_slices) table_checks(p, id - check0);
 
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanParams p) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    s_last = atomicAdd(&p.ctrl->done, 1u) == gridDim.x - 1;
+    s_last = atomicAdd(&p.ctrl->done, 1u) == (unsigned)p.n_counted - 1;
     if (s_last) __threadfence();
   }
   __syncthreads();
@@ -393,10 +397,9 @@ __global__ void __launch_bounds__(kTableEntries) phase_table_kernel(float4* out,
   const int e = blockIdx.x * kTableEntries + threadIdx.x;
   if (e >= n_entries) return;
   const int f = e / n_t, pp = e - f * n_t;
-  const double t = (double)(frame_lo + f);
-  const double delta = __dsub_rn(dev_phase(t, (double)q0, (double)T_s, R, S, g_mode), t);
-  const double theta = exp2(__dmul_rn(-(double)pp / (double)n_t, log2(base)));
-  out[e] = dev_trig_entry(__dmul_rn(theta, delta));
+  bool moves = false;
+  out[e] = dev_turn_entry((double)(frame_lo + f), pp, n_t, log2(base), (double)q0, (double)T_s, R, S, g_mode, false,
+                          &moves);
 }
 
 }  // namespace
@@ -413,7 +416,10 @@ cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
   const int checks = p.n_plane_slices > p.n_tbl_slices ? p.n_plane_slices : p.n_tbl_slices;
   int grid = p.n_tiles + p.n_trig_blocks + checks;
   if (grid < 1) grid = 1;
-  scan_kernel<<<grid, kThreads, 0, s>>>(p);
+  ScanParams q = p;
+  q.n_counted = grid - p.n_trig_blocks;  // tile and check CTAs; all CTAs when there are none
+  if (q.n_counted < 1) q.n_counted = grid;
+  scan_kernel<<<grid, kThreads, 0, s>>>(q);
   return cudaGetLastError();
 }
 

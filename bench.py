@@ -44,7 +44,7 @@ GATHER_TRAFFIC_SOURCES_SHA256 = "7a70e3aec16efe017e28ea5a7379fa510deefd84d5e8a0a
 def _gather_traffic():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gather.cu", "dcp_internal.cuh"):
+    for f in ("gather.cu", "rephase_body.cuh", "dcp_internal.cuh"):
         with open(os.path.join(ROOT, "autoregressive_video_diffusion_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return GATHER_TRAFFIC_BYTES if h.hexdigest() == GATHER_TRAFFIC_SOURCES_SHA256 else None
@@ -290,8 +290,9 @@ class FullDepthStep:
                                 kept_host, self.ws)
 
     def launches_per_step(self):
-        rephase = self.q0_prev != self.q0 and self.w.n_temporal_pairs > 0
-        return 3 if rephase else 2
+        """The scan, then one launch that moves the kept rows (with the history re-index folded in when there is one:
+        no static heads here)."""
+        return 2
 
 
 class PagedFullDepthStep(FullDepthStep):
@@ -991,6 +992,8 @@ def main():
                     help="profiling captures only: the same workload with fewer layers (a few GB on the device)")
     ap.add_argument("--tokens-per-frame", type=int, default=0,
                     help="profiling captures only: the same workload with shorter chunks (every plane kept, a few GB)")
+    ap.add_argument("--rotated", action="store_true",
+                    help="profiling captures only: the rotated full-depth eviction (every kept key turns) instead")
     ap.add_argument("--preroll", type=float, default=1.0, help="seconds of untimed steps before the timed region")
     ap.add_argument("--detail", default="", help="write the full result of every extra workload (curves, per-kernel "
                                                  "times) as JSON to this file; the line carries a compact summary")
@@ -1030,7 +1033,8 @@ def main():
         return
 
     from synth.workloads import FULL, FULL_ROTATED, scaled
-    w = FULL if args.layers <= 0 else scaled(FULL, L=args.layers, name=f"{FULL.name}_L{args.layers}")
+    base = FULL_ROTATED if args.rotated else FULL
+    w = base if args.layers <= 0 else scaled(base, L=args.layers, name=f"{base.name}_L{args.layers}")
     if args.tokens_per_frame > 0:
         T = args.tokens_per_frame
         w = scaled(w, tokens_per_frame=T, hist_cap=4 * T, name=f"{w.name}_T{T}")

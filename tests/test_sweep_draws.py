@@ -34,6 +34,22 @@ def test_sweep_draws_replay_in_the_oracle():
     assert all(v > 0 for v in seen.values()), seen
 
 
+def test_draws_reach_both_reindex_paths():
+    """Steps that re-index a history turn it in the gather's own launch when every plane receives, and in a re-index
+    kernel of its own before the gather when some heads are static: the narrow draws reach both."""
+    fused = separate = 0
+    for case in range(N_CASES):
+        w, over, hsm, _ = draw(case)
+        if over["reindex_mode"] == 1 or w.n_temporal_pairs == 0:
+            continue
+        T_s, end = w.sink_chunks * w.F, (w.S if w.g_mode == 0 else w.R + w.S)
+        for i, (c, q0_prev, q0) in enumerate(w.evictions()):
+            if i > 0 and q0 != q0_prev and (q0 - T_s > end or q0_prev - T_s > end):  # history keys turn
+                separate += hsm is not None
+                fused += hsm is None
+    assert fused > 0 and separate > 0, (fused, separate)
+
+
 def test_wide_draws_replay_in_the_oracle():
     """The wide draws (1024+ planes, rows of at most 288 bytes) replay in the oracle, and some of their steps turn no
     kept key (the staged gather) while others turn (the register-staged one)."""
