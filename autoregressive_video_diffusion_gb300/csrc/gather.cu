@@ -197,7 +197,9 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(const GatherParams 
 // kernel's ramp and tail.  Measured against the two kernels (mid eviction; last ten steps of the eager minute
 // rollout): 45.1 vs 48.1 us and 1114.5 vs 1122.3 us with the gather first and four planes in flight per re-index
 // thread; the re-index first measured 1118.5 us, six planes in flight 1138-1150 us, and three CTAs per SM (the
-// re-index kernel's own occupancy, with a gather that holds one plane at a time) 1199.8 us.
+// re-index kernel's own occupancy, with a gather that holds one plane at a time) 1199.8 us.  The re-index here keeps
+// the next group of four planes' loads in flight while a group is turned and stored (two register sets in turn):
+// rollout 1096.6-1097.8 vs 1109.9-1110.9 us without (two planes per group: 1262.6 us).
 constexpr int kFusedPlanesInFlight = 4;
 
 template <int NW, bool PAGED>
@@ -211,8 +213,9 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const GatherParams gp
   if (rp_max > 0 && rp.nvt > 0) {
     int rows_per_item = 0;
     const int64_t units = rephase_unit_count(rp, rp_max, &rows_per_item);
-    rephase_units<NW, PAGED, kFusedPlanesInFlight>(rp, rp_max, rows_per_item, rp_max, units * blockIdx.x / gridDim.x,
-                                                   units * (blockIdx.x + 1) / gridDim.x);
+    rephase_units<NW, PAGED, kFusedPlanesInFlight, true>(rp, rp_max, rows_per_item, rp_max,
+                                                         units * blockIdx.x / gridDim.x,
+                                                         units * (blockIdx.x + 1) / gridDim.x);
   }
 }
 

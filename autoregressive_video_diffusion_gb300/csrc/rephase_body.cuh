@@ -20,8 +20,9 @@ __device__ __forceinline__ int64_t rephase_unit_count(const RephaseParams& p, in
 // Re-index units [u_begin, u_end) of the (row block, plane) grid, block-major: a CTA's contiguous share.  Every
 // thread of the CTA must call it (it synchronises the CTA once per row block).  uniform_len >= 0: every plane's
 // history before the step has that many rows (the fused kernel, whose gather grows hist_len while this runs);
-// uniform_len < 0: each plane's length is read from hist_len.  PIF planes are loaded before any is stored.
-template <int NW, bool PAGED, int PIF>
+// uniform_len < 0: each plane's length is read from hist_len.  PIF planes are loaded before any is stored; with PIPE
+// the next PIF planes' loads are also in flight while a group is turned and stored (twice the registers).
+template <int NW, bool PAGED, int PIF, bool PIPE = false>
 __device__ __forceinline__ void rephase_units(const RephaseParams& p, int rp_max, int rows_per_item, int uniform_len,
                                               int64_t u_begin, int64_t u_end) {
   using Off = typename std::conditional<PAGED, int64_t, int>::type;
@@ -66,21 +67,45 @@ __device__ __forceinline__ void rephase_units(const RephaseParams& p, int rp_max
     else
       off = row * p.row_bytes + vec * VB;
 
-    for (int pl = p0; pl < p1; pl += PIF) {
-      Vec<NW> x[PIF];
-      bool go[PIF];
+    auto load_group = [&](int pl, Vec<NW>(&x)[PIF], bool(&go)[PIF]) {
 #pragma unroll
       for (int q = 0; q < PIF; ++q) {
         const int plq = pl + q;
         go[q] = live && plq < p1 && row < (uniform_len >= 0 ? uniform_len : __ldg(p.hist_len + min(plq, p1 - 1)));
         if (go[q]) ld_plain(x[q], p.k + plane_base(plq) + hist0 + off);
       }
+    };
+    auto store_group = [&](int pl, Vec<NW>(&x)[PIF], const bool(&go)[PIF]) {
 #pragma unroll
       for (int q = 0; q < PIF; ++q) {
         if (go[q]) {
           dev_rotate_vec_regs(x[q], p.dtype, vec * ppv, p.n_t, tr);
           st_plain(p.k + plane_base(pl + q) + hist0 + off, x[q]);
         }
+      }
+    };
+    if (!PIPE) {
+      for (int pl = p0; pl < p1; pl += PIF) {
+        Vec<NW> x[PIF];
+        bool go[PIF];
+        load_group(pl, x, go);
+        store_group(pl, x, go);
+      }
+    } else {
+      // two register sets in turn: the next group's loads are issued before this group is turned and stored, and
+      // no register holding a load in flight is ever copied (a copy would wait for the load)
+      Vec<NW> xa[PIF], xb[PIF];
+      bool ga[PIF], gb[PIF];
+      int pl = p0;
+      if (pl < p1) load_group(pl, xa, ga);
+      while (pl < p1) {
+        if (pl + PIF < p1) load_group(pl + PIF, xb, gb);
+        store_group(pl, xa, ga);
+        pl += PIF;
+        if (pl >= p1) break;
+        if (pl + PIF < p1) load_group(pl + PIF, xa, ga);
+        store_group(pl, xb, gb);
+        pl += PIF;
       }
     }
   }

@@ -34,17 +34,19 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-# DRAM bytes (read + write) of one full-depth gather launch, from an ncu capture of dram__bytes_read.sum and
-# dram__bytes_write.sum on the same kernel.  They describe the kernel sources they were taken on: when the hash of
-# those sources differs, the bench reports no traffic figure.
-GATHER_TRAFFIC_BYTES = 1_503_282_432
-GATHER_TRAFFIC_SOURCES_SHA256 = "7a70e3aec16efe017e28ea5a7379fa510deefd84d5e8a0ad0270183ab437f884"
+# DRAM bytes (read + write) of one full-depth gather launch (gather_staged_kernel<false>), scaled from ncu captures of
+# dram__bytes_read.sum and dram__bytes_write.sum on two reduced cases of the same workload (156 and 312 tokens per
+# frame): reads scale with the algorithmic reads (1.0006x), writes are the algorithmic writes less the ~50 MB still
+# dirty in L2 when the launch ends.  They describe the kernel sources they were taken on (gather.cu and the shared
+# header): when the hash of those sources differs, the bench reports no traffic figure.
+GATHER_TRAFFIC_BYTES = 1_501_890_646
+GATHER_TRAFFIC_SOURCES_SHA256 = "b33453cf9391b10a7da1788087a69a6041a104bdd85fda78d75819ce4091ef96"
 
 
 def _gather_traffic():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gather.cu", "rephase_body.cuh", "dcp_internal.cuh"):
+    for f in ("gather.cu", "dcp_internal.cuh"):
         with open(os.path.join(ROOT, "autoregressive_video_diffusion_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return GATHER_TRAFFIC_BYTES if h.hexdigest() == GATHER_TRAFFIC_SOURCES_SHA256 else None
@@ -998,13 +1000,14 @@ def main():
     ap.add_argument("--detail", default="", help="write the full result of every extra workload (curves, per-kernel "
                                                  "times) as JSON to this file; the line carries a compact summary")
     ap.add_argument("--case", default="step",
-                    choices=["step", "reindex", "score", "random", "read", "snapshot", "paged-hnd", "paged-nhd"],
+                    choices=["step", "reindex", "score", "random", "read", "snapshot", "paged-hnd", "paged-nhd", "mid"],
                     help="step: the prune step (default); reindex: dcp_rope_reindex of a 64-plane cache with 90,000 "
                          "history rows per plane; score: dcp_score_mask of one full-depth chunk (random: under "
                          "keep rule 2); read: dcp_read_history_keys of the re-index case's history; snapshot: "
                          "dcp_snapshot / dcp_restore of the state after the full-depth eviction cut to --layers "
                          "(default 8) layers; paged-hnd / paged-nhd: the full-depth step on a paged copy of the "
-                         "cache (16-position blocks)")
+                         "cache (16-position blocks); mid: the mid bf16 eviction (history of five chunks built by the "
+                         "library, re-indexed 36 -> 40 in the gather's launch), --steps repetitions")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1027,6 +1030,12 @@ def main():
                           "us_per_step": r["ms"] * 1e3, "GB_per_s": r["alg_bytes"] / (r["ms"] * 1e-3) / 1e9,
                           "gather_us": r["gather_ms"] * 1e3,
                           "gather_GB_per_s": r["gather_bytes"] / (r["gather_ms"] * 1e-3) / 1e9}))
+        return
+    if args.case == "mid":
+        import __graft_entry__
+        __graft_entry__.build()
+        from synth.workloads import MID
+        print(json.dumps({"case": "mid", **run_last_eviction(MID, reps=args.steps)}))
         return
     if args.case != "step":
         run_entry_case(args.case, args.steps, args.warmup)
