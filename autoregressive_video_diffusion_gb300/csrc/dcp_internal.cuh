@@ -324,6 +324,20 @@ __device__ __forceinline__ float4 dev_turn_entry(double t, int pp, int n_t, doub
   return dev_trig_entry(__dmul_rn(theta, delta));
 }
 
+// Table entry of a history key's re-index when the query frame moves from q0_prev to q0: the turn of pair pp from
+// t~(t; q0_prev) to t~(t; q0); *moves: the two phases differ.  (A step kernel whose CTAs each built the entries of
+// their own frames with it, so as to re-index before the scan completes, measured slower: each CTA waited on one
+// fp64 chain of GB300's low fp64 rate first; mid eviction 53.1 vs 45.4 us.)
+__device__ __forceinline__ float4 dev_reindex_entry(double t, int pp, int n_t, double log2_base, double q0_prev,
+                                                    double q0, double T_s, double R, double S, int mode, bool* moves) {
+  const double before = dev_phase(t, q0_prev, T_s, R, S, mode);
+  const double after = dev_phase(t, q0, T_s, R, S, mode);
+  const double delta = __dsub_rn(after, before);
+  const double theta = exp2(__dmul_rn(-(double)pp / (double)n_t, log2_base));
+  *moves = after != before;
+  return dev_trig_entry(__dmul_rn(theta, delta));
+}
+
 // Rotate one pair (a, b) of fp32 values by the angle whose cos/sin pairs are in t:
 //   out_a = a*c - b*s, out_b = a*s + b*c.
 // The rounding error of the b-products is recovered exactly with an fma and the low parts of cos/sin are added, so

@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kThreads) gather_staged_kernel(const GatherPar
       c_dst[u] = 0;
       if (u < kMaxTurnChunks) c_rot[u] = -1;
       if (u >= per_thread) continue;
-      if (!TURN) {
+      if constexpr (!TURN) {
         const int t = e >= chunks;  // tensor: K, then V
         const int ci = e - t * chunks;
         if (ci < nchunks) {

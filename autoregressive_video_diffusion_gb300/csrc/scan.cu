@@ -199,12 +199,10 @@ __device__ void table_work(const ScanParams& p, int block) {
     const int e2 = e - n_g;
     const int f = e2 / p.n_t, pp = e2 - f * p.n_t;
     const int t = p.h_lo + f;
-    const double before = dev_phase((double)t, (double)p.q0_prev, (double)p.T_s, p.R, p.S, p.g_mode);
-    const double after = dev_phase((double)t, (double)p.q0, (double)p.T_s, p.R, p.S, p.g_mode);
-    const double delta = __dsub_rn(after, before);
-    const double theta = exp2(__dmul_rn(-(double)pp / (double)p.n_t, log2_base));
-    p.trig_h[(int64_t)t * p.n_t + pp] = dev_trig_entry(__dmul_rn(theta, delta));
-    if (pp == 0) p.rot_h[t] = after != before;
+    bool moves = false;
+    p.trig_h[(int64_t)t * p.n_t + pp] = dev_reindex_entry((double)t, pp, p.n_t, log2_base, (double)p.q0_prev,
+                                                          (double)p.q0, (double)p.T_s, p.R, p.S, p.g_mode, &moves);
+    if (pp == 0) p.rot_h[t] = moves ? 1 : 0;
   }
 }
 
