@@ -2,8 +2,8 @@
 
 The paged layout is a bijection of rows (tests/paged.py packs a contiguous cache into seeded, shuffled blocks and
 reads it back), so the bars are those of the contiguous step: masks, indices, hist_len, hist_t, values and
-non-temporal key dims bit-exact, re-phased keys within 1 bf16 ulp (2 fp32 ulp) of the oracle; in addition free
-blocks are never written.
+non-temporal key dims bit-exact, re-phased keys within 1 bf16 ulp (fp32: 2 ulp plus 2^-38 of the pair) of the oracle;
+in addition free blocks are never written.
 """
 import numpy as np
 import pytest

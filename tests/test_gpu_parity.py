@@ -1,8 +1,8 @@
 """GPU parity: the CUDA prune step (through the C ABI) against the CPU oracle on the same seeded inputs.
 
-Bars: masks, index lists, kept counts, hist_len, hist_t, every value row and every
-non-temporal key dim are bit-exact; l is within 1e-5 relative; re-phased keys are within 1 bf16 ulp (2 fp32 ulp) of
-the oracle's fp64 rotation rounded once.  The masks are compared exactly because every seeded input keeps
+Bars: masks, index lists, kept counts, hist_len, hist_t, every value row and every non-temporal key dim are bit-exact;
+l is within 1e-5 relative; re-phased keys are within 1 bf16 ulp (fp32 keys: 2 ulp plus 2^-38 of the pair's |a| + |b|)
+of the oracle's fp64 rotation rounded once.  The masks are compared exactly because every seeded input keeps
 |l - gamma| >= 1e-6 (checked on the CPU in test_abi.py).
 """
 import numpy as np
@@ -35,14 +35,30 @@ def assert_score_parity(g_ell, ell, g_mask, mask, g_idx, idx, kept):
     assert np.array_equal(g_idx[:kept].cpu().numpy(), idx)
 
 
+FP32_TURN_ABS = 2.0 ** -38  # absolute error of the fp32 turn, in units of the pair's |a| + |b|
+
+
 def assert_key_parity(g: np.ndarray, o: np.ndarray, n_t: int) -> int:
-    """Temporal dims within 1 bf16 ulp (2 fp32 ulp) of the oracle; the rest bitwise.  Returns the count of entries
-    that are not bit-exact."""
+    """Temporal dims within 1 bf16 ulp of the oracle (bf16 keys), or within 2 fp32 ulp plus 2^-38 of the pair's
+    |a| + |b| (fp32 keys); the rest bitwise.  Returns the count of entries that are not bit-exact.
+
+    The fp32 bound is the turn's own error: the cos/sin table carries ~40 significant bits, so an output that nearly
+    cancels (a cos - b sin far below the pair's length) keeps an absolute error of ~2^-40 of the pair, which is many
+    of its own ulps; elsewhere the relative error of the few rounded operations stays within 2 ulp."""
     nt2 = 2 * n_t
     assert np.array_equal(g[..., nt2:], o[..., nt2:]), "non-temporal key dims must be copied bitwise"
-    tol = 1 if g.dtype == np.uint16 else 2
     d = replay.ulp_distance(g[..., :nt2], o[..., :nt2])
-    assert int(d.max(initial=0)) <= tol, f"re-phased key off by {int(d.max())} ulp"
+    if g.dtype == np.uint16:
+        assert int(d.max(initial=0)) <= 1, f"re-phased key off by {int(d.max())} ulp"
+    else:
+        gv = g[..., :nt2].view(np.float32).astype(np.float64)
+        ov = o[..., :nt2].view(np.float32)
+        pair = np.abs(ov.astype(np.float64)).reshape(ov.shape[:-1] + (n_t, 2)).sum(-1).repeat(2, axis=-1)
+        bound = 2 * np.spacing(np.abs(ov)).astype(np.float64) + FP32_TURN_ABS * pair
+        err = np.abs(gv - ov.astype(np.float64))
+        bad = err > bound
+        assert not bad.any(), (f"re-phased fp32 key off by {int(d[bad].max())} ulp, "
+                               f"{(err[bad] / pair[bad]).max():.3g} of the pair's |a| + |b|")
     return int(np.count_nonzero(d))
 
 

@@ -2,8 +2,8 @@
 
 Section "what differs" of the DeCoPrune page: history keys take t~(t; q0); with read-time re-index they stay at their
 own frame's phase, move bitwise, and are turned once when read.  Bars: a prune step in this mode is bit-exact
-(nothing rotates); a read is within 1 bf16 ulp (2 fp32 ulp) of the oracle's fp64 turn of the stored key, other dims
-bitwise, and rows past a plane's history are not written.
+(nothing rotates); a read is within 1 bf16 ulp (fp32: 2 ulp plus 2^-38 of the pair) of the oracle's fp64 turn of the
+stored key, other dims bitwise, and rows past a plane's history are not written.
 """
 import numpy as np
 import pytest

@@ -1,6 +1,6 @@
 """Seeded sweep of small geometries: every eviction of each drawn workload runs on the GPU and in the oracle from the
 same host state, with the bars of test_gpu_parity.py (masks, indices, lengths, frames, values and non-temporal key
-dims bit-exact; turned key dims within 1 bf16 ulp or 2 fp32 ulp).
+dims bit-exact; turned key dims within 1 bf16 ulp, or 2 fp32 ulp plus 2^-38 of the pair).
 
 The draws cover what the fixed cases leave at one value: bf16 and fp32 rows of 16 to 544 bytes (16-byte vectors when a
 row is not a multiple of 32 bytes), 0 to D/2 temporal pairs, ragged chunks (3 to 64 tokens per frame, 1 to 3 frames),
@@ -13,7 +13,8 @@ shared-memory staged gather, across row sizes and dtypes, and steps that turn on
 them run on paged pools (HND or NHD, 8 to 32 positions per block), which take the register-staged gather.  Big
 draws use rows of 1 to 4 KiB (the largest the library takes) with up to 1024 temporal pairs; edge draws use chunks of
 1 to 33 tokens and score rows of 1 to 64 values.  Boundary draws put the last eviction exactly on the edge of g's
-identity on the leaving chunk (where the library skips the chunk's turn) and one frame past it, for both maps g.
+identity on the leaving chunk (where the library skips the chunk's turn) and one frame past it, for both maps g;
+staged-turn draws put steps whose keys turn on the staged gather's turning form in bf16 and fp32.
 """
 import numpy as np
 import pytest
@@ -196,16 +197,47 @@ def draw_boundary(case: int):
 N_BOUNDARY = len(BOUNDARY)
 
 
+def draw_staged_turn(case: int):
+    """A 1024-plane cache (bf16 and fp32 in turn, rows of 64 to 256 bytes) whose last eviction turns its kept keys
+    while every row holds 1 to 8 temporal 16-byte chunks: the staged gather's turning form, across both dtypes (the
+    compensated fp32 turn included), row sizes, temporal extents, and kept counts from part of one 64-row block to
+    several blocks."""
+    r = np.random.default_rng(0x57A6 + case)
+    dtype = case % 2
+    D = int(r.choice([32, 64, 128] if dtype == 0 else [16, 32, 64]))
+    ppv = 4 if dtype == 0 else 2                          # rotary pairs per 16-byte chunk
+    tc = int(r.integers(1, min(8, D * (2 if dtype == 0 else 4) // 16) + 1))
+    n_t = min(D // 2, tc * ppv - int(r.integers(0, ppv)))
+    F, T = int(r.integers(1, 4)), int(r.choice([16, 40, 64]))
+    sink, win, n_ev = 1, int(r.integers(1, 3)), int(r.integers(2, 4))
+    last = sink + n_ev - 1
+    R = win * F                                           # the leaving chunk's oldest offset (w + 1) F lies past R
+    S = R + int(r.integers(0, 2))                         # g compresses once q0 - T_s > S
+    w = scaled(TINY, name=f"sweep_staged_turn_{case}", index=600 + case, L=32, H=32, D=D, dtype=dtype,
+               n_temporal_pairs=n_t, rope_base=1e4, tokens_per_frame=T, frames_per_chunk=F, d=16, sink_chunks=sink,
+               window_chunks=win, R=float(R), S=float(S), g_mode=0, hist_cap=n_ev * T * F,
+               max_frames=(last + win + 2) * F, evict_chunk=last, history_chunks=tuple(range(sink, last)),
+               seed=9800 + case)
+    while not _clear_of_tie_band(w):
+        w = scaled(w, seed=w.seed + 100)
+    return w, {"keep_rule": int(r.choice([0, 1])), "random_seed": 0, "reindex_mode": 0}, None, None
+
+
+N_STAGED_TURN = 6
+
+
 @pytest.mark.parametrize("case", [("narrow", i) for i in range(N_CASES)] + [("wide", i) for i in range(N_WIDE)] +
                          [("big", i) for i in range(N_BIG)] + [("edge", i) for i in range(N_EDGE)] +
-                         [("boundary", i) for i in range(N_BOUNDARY)],
+                         [("boundary", i) for i in range(N_BOUNDARY)] +
+                         [("staged_turn", i) for i in range(N_STAGED_TURN)],
                          ids=[f"case{i}" for i in range(N_CASES)] + [f"wide{i}" for i in range(N_WIDE)] +
                          [f"big{i}" for i in range(N_BIG)] + [f"edge{i}" for i in range(N_EDGE)] +
-                         [f"boundary_m{m}_{b}_{sd}" for m, b, sd in BOUNDARY])
+                         [f"boundary_m{m}_{b}_{sd}" for m, b, sd in BOUNDARY] +
+                         [f"staged_turn{i}" for i in range(N_STAGED_TURN)])
 def test_sweep_case(gpu, case):
     kind, case = case
     w, over, hsm, paged = {"narrow": draw, "wide": draw_wide, "big": draw_big, "edge": draw_edge,
-                           "boundary": draw_boundary}[kind](case)
+                           "boundary": draw_boundary, "staged_turn": draw_staged_turn}[kind](case)
     ocfg = replay.cfg_of(w)
     for key, val in over.items():
         setattr(ocfg, key, val)

@@ -4,8 +4,8 @@ import numpy as np
 
 from oracle import replay
 import oracle
-from tests.test_gpu_sweep import (BOUNDARY, N_BIG, N_BOUNDARY, N_CASES, N_EDGE, N_WIDE, draw, draw_big, draw_boundary,
-                                  draw_edge, draw_wide)
+from tests.test_gpu_sweep import (BOUNDARY, N_BIG, N_BOUNDARY, N_CASES, N_EDGE, N_STAGED_TURN, N_WIDE, draw, draw_big,
+                                  draw_boundary, draw_edge, draw_staged_turn, draw_wide)
 
 
 def test_sweep_draws_replay_in_the_oracle():
@@ -122,3 +122,27 @@ def test_boundary_draws_turn_exactly_past_the_boundary():
         moved = hc.k[:, :, w.sink_rows + common: w.sink_rows + common + len(idx)]
         same = np.array_equal(moved, src[:, :, idx])
         assert same == (side == "at"), (case, BOUNDARY[case])
+
+
+def test_staged_turn_draws_reach_the_turning_staged_gather():
+    """The staged-turn draws are valid, and their last eviction meets every condition under which the library takes
+    the staged gather's turning form (1024+ planes, rows of at most 288 bytes, at most 8 temporal 16-byte chunks per
+    row, kept keys that turn), in both dtypes, with kept counts that fill part of one 64-row block and several."""
+    dtypes, ks = set(), []
+    for case in range(N_STAGED_TURN):
+        w, over, hsm, paged = draw_staged_turn(case)
+        ppv = 4 if w.dtype == 0 else 2
+        tc = -(-w.n_temporal_pairs // ppv)
+        assert paged is None and hsm is None and w.n_planes >= 1024 and w.D * w.esize <= 288 and 1 <= tc <= 8
+        cfg = replay.cfg_of(w)
+        for key, val in over.items():
+            setattr(cfg, key, val)
+        hc, (c, q0_prev, q0) = replay.state_before_last(w, cfg=cfg)
+        T_s = w.sink_chunks * w.F
+        assert q0 - T_s > w.S and q0 - w.first_frame(c) > w.R  # the last eviction's oldest frame turns
+        rc, _, _, idx = oracle.prune_step(hc, cfg, *w.score_inputs(c), w.slot_of(c), w.first_frame(c), q0_prev, q0)
+        assert rc == oracle.OK and len(idx) > 0
+        dtypes.add(w.dtype)
+        ks.append(len(idx))
+    assert dtypes == {0, 1}, dtypes
+    assert min(ks) < 64 < max(ks) and any(k % 64 for k in ks), ks
