@@ -199,8 +199,8 @@ dcp_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? DCP_OK : DCP_ECUDA
 // holds when the oldest non-sink offset already fits the span (g is then the identity everywhere) or when the chunk's
 // oldest offset is within the recent range R.  Read-time re-index moves keys unturned.
 // This decision is load-bearing, not only a choice of speed: when it holds, the scan builds no cos/sin table for the
-// chunk and no gather form turns any key (the staged form cannot turn; the register-staged one skips its turn under
-// no_turn).  It is exact because it restates g's closed form: g(delta) = delta for delta <= R, and everywhere when
+// chunk and no gather form turns any key (the staged gather takes its copy-only form; the register-staged one skips
+// its turn under no_turn).  It is exact because it restates g's closed form: g(delta) = delta for delta <= R, and everywhere when
 // delta_max = q0 - T_s <= span end, so t~(t) = t for every frame of the chunk (the chunk's oldest offset is
 // q0 - evict_first_frame, its largest).  The GPU sweep draws steps on both sides of each boundary
 // (q0 - evict_first_frame = R, R + 1; q0 - T_s = span end, span end + 1) and compares them with the oracle.

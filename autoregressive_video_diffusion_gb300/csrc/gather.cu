@@ -22,7 +22,8 @@
 // Bookkeeping folded in: the item holding the first block of a receiving plane sets its hist_len to
 // common_len + k, and the items of the lowest receiving plane append the kept frames to hist_t.
 //
-// A staged form (below) serves the steps in which no kept key turns, on caches of 1024 planes or more.
+// A staged form (below) serves contiguous caches of 1024 planes or more: a copy-only form for the steps in which no
+// kept key turns, and a form that turns the temporal chunks through registers for the others.
 //
 // Paged caches (block pools addressed through block tables) use the same decomposition: a thread's source and
 // destination offsets inside a plane come from the tables once per item, and a plane's base from its layer and head.
@@ -509,10 +510,11 @@ cudaError_t launch_step_fused(const GatherParams& gp, const RephaseParams& rp, c
 }
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t s, bool overlap_launch, bool paged) {
-  // the staged form when no kept key turns, the cache has many planes and two CTAs' stages fit in shared memory (bf16
-  // rows up to 256 bytes).  Measured on the full-depth eviction (1600 planes): step 248.1 vs 250.5 us; on the same
-  // eviction cut to 320 planes the register-staged kernel is faster (step 59.5 vs 64.0 us: items of a few planes
-  // spend much of their time filling and draining three stages).
+  // the staged form when the cache has many planes and two CTAs' stages fit in shared memory (rows up to 288 bytes;
+  // the turning form also needs at most two temporal chunks per thread).  Measured on the full-depth eviction (1600
+  // planes): step 248.1 vs 250.5 us copy-only, 255 vs 262 us when every key turns; on the same eviction cut to 320
+  // planes the register-staged kernel is faster (step 59.5 vs 64.0 us: items of a few planes spend much of their
+  // time filling and draining three stages).
   if (!paged && p.n_planes >= 1024 && p.row_bytes % 16 == 0 && p.row_bytes <= 288) {
     if (p.no_turn && staged_smem_bytes(p, false) <= 110 * 1024) return launch_staged<false>(p, s, overlap_launch);
     if (!p.no_turn && staged_turn_fits(p) && staged_smem_bytes(p, true) <= 110 * 1024)

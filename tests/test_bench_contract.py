@@ -90,3 +90,19 @@ def test_compact_extra_fits_the_kept_tail():
     assert abs(ex["mid_bf16"]["GB_per_s"] - 146e6 / 40e-6 / 1e9) <= 1
     text = json.dumps({"cpu_baseline": {"value": 1.07, "unit": "GB/s", "cores": 1, "kind": "oracle"}, "extra": ex})
     assert len(text) < 1400, len(text)
+
+
+def test_traffic_figure_keyed_to_code_not_comments():
+    """The bench keeps its DRAM-traffic figure only while the gather's code is the one the counters were taken on; the
+    key drops // comments and blank lines, which is sound only while the keyed sources hold no // inside a string
+    literal and no block comment."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench._code_only("a = 1;  // x\n\n  // y\n  b(2);   \n") == "a = 1;\n  b(2);"
+    for f in ("gather.cu", "dcp_internal.cuh"):
+        with open(os.path.join(ROOT, "autoregressive_video_diffusion_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        assert "/*" not in text, f
+        for ln in text.splitlines():
+            code = ln.split("//", 1)[0]
+            assert code.count('"') % 2 == 0, (f, ln)  # every string literal closes before a // on its line
