@@ -14,7 +14,8 @@ them run on paged pools (HND or NHD, 8 to 32 positions per block), which take th
 draws use rows of 1 to 4 KiB (the largest the library takes) with up to 1024 temporal pairs; edge draws use chunks of
 1 to 33 tokens and score rows of 1 to 64 values.  Boundary draws put the last eviction exactly on the edge of g's
 identity on the leaving chunk (where the library skips the chunk's turn) and one frame past it, for both maps g;
-staged-turn draws put steps whose keys turn on the staged gather's turning form in bf16 and fp32.
+staged-turn draws put steps whose keys turn on the staged gather's turning form in bf16 and fp32, with and without
+static heads.
 """
 import numpy as np
 import pytest
@@ -198,10 +199,12 @@ N_BOUNDARY = len(BOUNDARY)
 
 
 def draw_staged_turn(case: int):
-    """A 1024-plane cache (bf16 and fp32 in turn, rows of 64 to 256 bytes) whose last eviction turns its kept keys
-    while every row holds 1 to 8 temporal 16-byte chunks: the staged gather's turning form, across both dtypes (the
-    compensated fp32 turn included), row sizes, temporal extents, and kept counts from part of one 64-row block to
-    several blocks."""
+    """A 1024-plane cache (bf16 and fp32 in turn, rows of 64 to 256 bytes, 1 to 8 temporal 16-byte chunks per row)
+    whose evictions all turn their kept keys.  The first eviction (q0 unchanged, nothing to re-index) takes the
+    staged gather's turning form, across both dtypes (the compensated fp32 turn included), row sizes, temporal
+    extents, and kept counts from part of one 64-row block to several blocks; the later ones take the fused gather +
+    re-index launch.  Cases 6 and up also make 1 to 31 heads of every layer static: every eviction then takes the
+    turning staged form, walking the scan's list of receiving planes instead of every plane."""
     r = np.random.default_rng(0x57A6 + case)
     dtype = case % 2
     D = int(r.choice([32, 64, 128] if dtype == 0 else [16, 32, 64]))
@@ -220,10 +223,13 @@ def draw_staged_turn(case: int):
                seed=9800 + case)
     while not _clear_of_tie_band(w):
         w = scaled(w, seed=w.seed + 100)
-    return w, {"keep_rule": int(r.choice([0, 1])), "random_seed": 0, "reindex_mode": 0}, None, None
+    over = {"keep_rule": int(r.choice([0, 1])), "random_seed": 0, "reindex_mode": 0}
+    if case >= 6:
+        w = scaled(w, n_static_per_layer=int(r.integers(1, w.H)))
+    return w, over, w.head_is_static(), None
 
 
-N_STAGED_TURN = 6
+N_STAGED_TURN = 10
 
 
 @pytest.mark.parametrize("case", [("narrow", i) for i in range(N_CASES)] + [("wide", i) for i in range(N_WIDE)] +

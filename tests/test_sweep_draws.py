@@ -125,24 +125,43 @@ def test_boundary_draws_turn_exactly_past_the_boundary():
 
 
 def test_staged_turn_draws_reach_the_turning_staged_gather():
-    """The staged-turn draws are valid, and their last eviction meets every condition under which the library takes
-    the staged gather's turning form (1024+ planes, rows of at most 288 bytes, at most 8 temporal 16-byte chunks per
-    row, kept keys that turn), in both dtypes, with kept counts that fill part of one 64-row block and several."""
-    dtypes, ks = set(), []
+    """The staged-turn draws are valid, every eviction of them turns its kept keys, and the evictions that take the
+    staged gather's turning form (1024+ planes, rows of at most 288 bytes, at most 8 temporal 16-byte chunks per row;
+    no history re-index in the same step, i.e. q0 unchanged, or static heads, which never fuse the re-index into the
+    gather) cover both dtypes, kept counts that fill part of one 64-row block and several, and (cases 6 and up)
+    static heads next to receiving ones in every layer."""
+    dtypes, ks, hs_cases = set(), [], 0
     for case in range(N_STAGED_TURN):
         w, over, hsm, paged = draw_staged_turn(case)
         ppv = 4 if w.dtype == 0 else 2
         tc = -(-w.n_temporal_pairs // ppv)
-        assert paged is None and hsm is None and w.n_planes >= 1024 and w.D * w.esize <= 288 and 1 <= tc <= 8
+        assert paged is None and w.n_planes >= 1024 and w.D * w.esize <= 288 and 1 <= tc <= 8
+        assert (hsm is None) == (case < 6)
+        if hsm is not None:
+            per_layer = hsm.reshape(w.L, w.H).sum(axis=1)
+            assert np.all(per_layer >= 1) and np.all(per_layer < w.H)
+            hs_cases += 1
         cfg = replay.cfg_of(w)
         for key, val in over.items():
             setattr(cfg, key, val)
-        hc, (c, q0_prev, q0) = replay.state_before_last(w, cfg=cfg)
+        hc = replay.new_host_cache(w)
+        placed = set()
         T_s = w.sink_chunks * w.F
-        assert q0 - T_s > w.S and q0 - w.first_frame(c) > w.R  # the last eviction's oldest frame turns
-        rc, _, _, idx = oracle.prune_step(hc, cfg, *w.score_inputs(c), w.slot_of(c), w.first_frame(c), q0_prev, q0)
-        assert rc == oracle.OK and len(idx) > 0
+        staged = 0
+        for c, q0_prev, q0 in w.evictions():
+            for cc in w.resident_window(c):
+                if cc not in placed:
+                    replay.place_chunk(hc, w, cc)
+                    placed.add(cc)
+            assert q0 - T_s > w.S and q0 - w.first_frame(c) > w.R  # the leaving chunk's oldest frame turns
+            rc, _, _, idx = oracle.prune_step(hc, cfg, *w.score_inputs(c), w.slot_of(c), w.first_frame(c), q0_prev,
+                                              q0, head_is_static=hsm)
+            assert rc == oracle.OK and len(idx) > 0
+            if q0_prev == q0 or hsm is not None:
+                staged += 1
+                ks.append(len(idx))
+        assert staged >= 1, case
         dtypes.add(w.dtype)
-        ks.append(len(idx))
     assert dtypes == {0, 1}, dtypes
+    assert hs_cases == N_STAGED_TURN - 6
     assert min(ks) < 64 < max(ks) and any(k % 64 for k in ks), ks
