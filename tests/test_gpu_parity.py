@@ -473,11 +473,16 @@ def _subset_place(hc, w, planes, chunks):
                                      W.chunk_stream(c, what), w.C, p * w.C)
 
 
-def test_head_specialised_prefix_pass(gpu):
+# the same prefix pass with a span that compresses (S = 14 < q0 - T_s): both evictions turn their kept keys, and the
+# second re-indexes the first one's history, on the staged gather's turning form over the receiving-plane list
+HS_PREFIX_TURNING = scaled(HS_PREFIX, name="head_specialised_prefix_turning", S=14)
+
+
+@pytest.mark.parametrize("w", [HS_PREFIX, HS_PREFIX_TURNING], ids=["identity", "turning"])
+def test_head_specialised_prefix_pass(gpu, w):
     """Config of 40 x 40 heads, 20 static per layer (Streaming), prefix pruning over 6 observed chunks (x0hat = the
     clean chunk re-noised at tau*, scored against the clean chunk); chunks 1 and 2 leave the window.  Sampled planes
     are replayed by the oracle as a cache of their own (planes are independent once the mask is fixed)."""
-    w = HS_PREFIX
     static = w.head_is_static()
     assert static.reshape(w.L, w.H).sum(axis=1).tolist() == [20] * w.L
     stream = torch.cuda.current_stream().cuda_stream
@@ -514,6 +519,19 @@ def test_head_specialised_prefix_pass(gpu):
         assert np.array_equal(vh[l, h].cpu().numpy().view(np.uint16), sub.v[0, i])
         assert_key_parity(kh[l, h].cpu().numpy().view(np.uint16), sub.k[0, i], w.n_temporal_pairs)
     assert 0.2 < ks[0] / w.C < 0.3
+    # the turning variant really turns: a receiving plane's first history row differs from its source key row in the
+    # temporal dims (and only there)
+    i = 4                                   # the first receiving plane of the sample
+    assert static[planes[i]] == 0
+    c1 = w.evictions()[0][0]
+    src = np.zeros((1, w.cap, w.D), np.uint16)
+    synth.fill_rows_host(src, w.dtype, 1, w.cap, W.chunk_row0(w, c1), w.C, w.D, w.seed, W.chunk_stream(c1, W.S_K),
+                         w.C, planes[i] * w.C)
+    first = W.chunk_row0(w, c1) + int(oracle.indices(oracle.keep(oracle.score(*w.score_inputs(c1)), w.gamma))[0])
+    row, raw = sub.k[0, i, w.sink_rows], src[0, first]
+    nt2 = 2 * w.n_temporal_pairs
+    assert np.array_equal(row[nt2:], raw[nt2:])
+    assert np.array_equal(row[:nt2], raw[:nt2]) == (w is HS_PREFIX)
 
 
 # ------------------------------------------------------------------------------------------ rollout
