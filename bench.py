@@ -1007,14 +1007,17 @@ def main():
     ap.add_argument("--detail", default="", help="write the full result of every extra workload (curves, per-kernel "
                                                  "times) as JSON to this file; the line carries a compact summary")
     ap.add_argument("--case", default="step",
-                    choices=["step", "reindex", "score", "random", "read", "snapshot", "paged-hnd", "paged-nhd", "mid"],
+                    choices=["step", "reindex", "score", "random", "read", "snapshot", "paged-hnd", "paged-nhd", "mid",
+                             "rollout-late"],
                     help="step: the prune step (default); reindex: dcp_rope_reindex of a 64-plane cache with 90,000 "
                          "history rows per plane; score: dcp_score_mask of one full-depth chunk (random: under "
                          "keep rule 2); read: dcp_read_history_keys of the re-index case's history; snapshot: "
                          "dcp_snapshot / dcp_restore of the state after the full-depth eviction cut to --layers "
                          "(default 8) layers; paged-hnd / paged-nhd: the full-depth step on a paged copy of the "
                          "cache (16-position blocks); mid: the mid bf16 eviction (history of five chunks built by the "
-                         "library, re-indexed 36 -> 40 in the gather's launch), --steps repetitions")
+                         "library, re-indexed 36 -> 40 in the gather's launch), --steps repetitions; rollout-late: the "
+                         "last eviction of the eager minute rollout cut to --layers (default 4) layers, its history "
+                         "built by the library over the 55 earlier evictions, --steps repetitions")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1043,6 +1046,13 @@ def main():
         __graft_entry__.build()
         from synth.workloads import MID
         print(json.dumps({"case": "mid", **run_last_eviction(MID, reps=args.steps)}))
+        return
+    if args.case == "rollout-late":
+        import __graft_entry__
+        __graft_entry__.build()
+        from synth.workloads import ROLLOUT, scaled
+        wr = scaled(ROLLOUT, L=args.layers or 4, name=f"{ROLLOUT.name}_L{args.layers or 4}")
+        print(json.dumps({"case": "rollout-late", **run_last_eviction(wr, reps=args.steps)}))
         return
     if args.case != "step":
         run_entry_case(args.case, args.steps, args.warmup)
