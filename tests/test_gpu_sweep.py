@@ -32,7 +32,7 @@ from tests.test_gpu_parity import assert_key_parity, gpu_vs_oracle_step
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 48
+N_CASES = 128
 
 
 def _clear_of_tie_band(w) -> bool:
@@ -106,7 +106,7 @@ def draw_wide(case: int):
     return w, over, w.head_is_static(), paged
 
 
-N_WIDE = 8
+N_WIDE = 16
 
 
 def draw_big(case: int):
@@ -133,7 +133,7 @@ def draw_big(case: int):
     return w, over, None, None
 
 
-N_BIG = 6
+N_BIG = 10
 
 # degenerate chunks: (tokens per frame, frames per chunk, score width)
 EDGE = [(1, 1, 1), (1, 3, 2), (2, 1, 3), (31, 1, 4), (33, 1, 5), (1, 2, 64)]
